@@ -1,0 +1,32 @@
+// Compiled kernel variants for f32 (float): register-tile geometries (P, S) and blocked
+// panel widths. The dispatcher picks among them; see dispatch.cpp.
+#include "launch.cuh"
+
+namespace bl {
+
+static const KernelEntry k_entries_f32[] = {
+    tile_entry<float, 2, 2>(),
+    tile_entry<float, 2, 4>(),
+    tile_entry<float, 4, 3>(),
+    tile_entry<float, 4, 4>(),
+    tile_entry<float, 4, 6>(),
+    tile_entry<float, 4, 8>(),
+    tile_entry<float, 4, 9>(),
+    tile_entry<float, 8, 5>(),
+    tile_entry<float, 8, 6>(),
+    tile_entry<float, 8, 8>(),
+    tile_entry<float, 8, 9>(),
+    tile_entry<float, 16, 6>(),
+    tile_entry<float, 16, 8>(),
+    tile_entry<float, 16, 9>(),
+    tile_entry<float, 16, 10>(),
+    blocked_entry<float, 32>(),
+    blocked_entry<float, 64>(),
+};
+
+const KernelEntry *entries_f32(int *count) {
+    *count = static_cast<int>(sizeof(k_entries_f32) / sizeof(k_entries_f32[0]));
+    return k_entries_f32;
+}
+
+}  // namespace bl

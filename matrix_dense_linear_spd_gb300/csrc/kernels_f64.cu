@@ -1,0 +1,31 @@
+// Compiled kernel variants for f64 (double): register-tile geometries (P, S) and blocked
+// panel widths. The dispatcher picks among them; see dispatch.cpp.
+#include "launch.cuh"
+
+namespace bl {
+
+static const KernelEntry k_entries_f64[] = {
+    tile_entry<double, 2, 2>(),
+    tile_entry<double, 2, 4>(),
+    tile_entry<double, 4, 3>(),
+    tile_entry<double, 4, 4>(),
+    tile_entry<double, 4, 5>(),
+    tile_entry<double, 4, 6>(),
+    tile_entry<double, 4, 8>(),
+    tile_entry<double, 4, 9>(),
+    tile_entry<double, 8, 5>(),
+    tile_entry<double, 8, 6>(),
+    tile_entry<double, 8, 8>(),
+    tile_entry<double, 8, 9>(),
+    tile_entry<double, 16, 6>(),
+    tile_entry<double, 16, 8>(),
+    blocked_entry<double, 16>(),
+    blocked_entry<double, 32>(),
+};
+
+const KernelEntry *entries_f64(int *count) {
+    *count = static_cast<int>(sizeof(k_entries_f64) / sizeof(k_entries_f64[0]));
+    return k_entries_f64;
+}
+
+}  // namespace bl

@@ -1,0 +1,61 @@
+// Launch helpers and the registry entry type shared by the per-dtype instantiation files.
+#pragma once
+
+#include <atomic>
+#include <cuda_runtime.h>
+
+#include "bl_types.cuh"
+#include "registry.h"
+#include "blocked_kernel.cuh"
+#include "tile_kernel.cuh"
+
+namespace bl {
+
+// Raise the dynamic shared-memory limit once per device for kernels above 48 KB.
+template <typename K>
+inline cudaError_t ensure_smem(K kern, size_t bytes, std::atomic<unsigned long long> &done) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+template <typename T, int P, int S>
+cudaError_t launch_tile(const BatchArgs &a, cudaStream_t st) {
+    using C = TileCfg<T, P, S>;
+    static std::atomic<unsigned long long> done{0};
+    cudaError_t e = ensure_smem(tile_kernel<T, P, S>, C::smem_bytes, done);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>((a.batch + C::G - 1) / C::G);
+    tile_kernel<T, P, S><<<grid, C::THREADS, C::smem_bytes, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int NB>
+cudaError_t launch_blocked(const BatchArgs &a, cudaStream_t st) {
+    using C = BlkCfg<T, NB>;
+    static std::atomic<unsigned long long> done{0};
+    cudaError_t e = ensure_smem(blocked_kernel<T, NB>, C::smem_bytes, done);
+    if (e != cudaSuccess) return e;
+    blocked_kernel<T, NB><<<static_cast<unsigned>(a.batch), C::THREADS, C::smem_bytes, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int P, int S>
+constexpr KernelEntry tile_entry() {
+    using C = TileCfg<T, P, S>;
+    return KernelEntry{0, P, S, 0, C::N, P, C::THREADS, C::G, C::smem_bytes, &launch_tile<T, P, S>};
+}
+
+template <typename T, int NB>
+constexpr KernelEntry blocked_entry() {
+    using C = BlkCfg<T, NB>;
+    return KernelEntry{1, 0, 0, NB, 0, 0, C::THREADS, 1, C::smem_bytes, &launch_blocked<T, NB>};
+}
+
+}  // namespace bl

@@ -1,0 +1,28 @@
+// Host-side description of one compiled kernel variant (plain data; no device code).
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "bl_types.cuh"
+
+namespace bl {
+
+// `cap` is the largest n + rhs-rows-per-pass the variant holds (0: any order); `rhs_max` the
+// right-hand sides one pass solves (0: any).
+struct KernelEntry {
+    int family;          // 0 = tile, 1 = blocked
+    int p, s, nb;        // tile geometry (p, s) or panel width nb
+    int cap;
+    int rhs_max;
+    int threads, per_cta;
+    size_t smem;
+    cudaError_t (*launch)(const BatchArgs &, cudaStream_t);
+};
+
+const KernelEntry *entries_f32(int *count);
+const KernelEntry *entries_f64(int *count);
+const KernelEntry *entries_c64(int *count);
+const KernelEntry *entries_c128(int *count);
+
+}  // namespace bl
