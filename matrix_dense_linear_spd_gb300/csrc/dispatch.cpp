@@ -74,6 +74,7 @@ std::vector<const KernelEntry *> candidates(int dtype) {
 std::string spelling(const KernelEntry &e) {
     char buf[64];
     if (e.family == 0) snprintf(buf, sizeof buf, "tile:p=%d:s=%d", e.p, e.s);
+    else if (e.family == 2) snprintf(buf, sizeof buf, "warp:p=%d:r=%d", e.p, e.s);
     else snprintf(buf, sizeof buf, "blocked:nb=%d", e.nb);
     return buf;
 }
@@ -92,7 +93,7 @@ std::string canon(std::string s) {
     while (std::getline(ss, tok, ':')) parts.push_back(tok);
     if (parts.empty()) return s;
     static const std::map<std::string, std::vector<std::string>> fields = {
-        {"tile", {"p", "s"}}, {"blocked", {"nb"}}};
+        {"tile", {"p", "s"}}, {"warp", {"p", "r"}}, {"blocked", {"nb"}}};
     auto it = fields.find(parts[0]);
     if (it == fields.end()) return s;
     std::string out = parts[0];
@@ -135,13 +136,14 @@ bool device_facts(DeviceFacts &f) {
 
 // Right-hand sides one pass of `e` takes, and whether the variant can run the shape at all.
 int rhs_per_pass(const KernelEntry &e, int op, int64_t nrhs) {
-    if (op == OP_POTRF) return 0;
+    if (op == OP_POTRF || e.rhs_max < 0) return 0;
     if (e.family == 1) return static_cast<int>(nrhs);
     return static_cast<int>(std::min<int64_t>(nrhs, e.rhs_max));
 }
 
 bool can_run(const KernelEntry &e, int op, int64_t n, int64_t nrhs, const DeviceFacts &dev) {
     if (e.smem > dev.smem_optin) return false;
+    if (op != OP_POTRF && e.rhs_max < 0) return false;  // factor-only variant
     if (e.family == 1) return true;
     return n + rhs_per_pass(e, op, nrhs) <= e.cap;
 }
@@ -336,11 +338,14 @@ bl_status choose_on(const DeviceFacts &dev, int op, int dtype, int uplo, int64_t
                     }
         }
     }
-    // last resort: the smallest register tile that holds the shape, else the blocked family
+    // last resort: the smallest register-resident variant (warp or tile) that holds the shape,
+    // preferring the warp family on a tie, else the blocked family
     const KernelEntry *best = nullptr;
     for (const KernelEntry *e : cands) {
-        if (e->family != 0 || !can_run(*e, op, n, nrhs, dev)) continue;
-        if (!best || e->cap < best->cap || (e->cap == best->cap && e->p > best->p)) best = e;
+        if (e->family == 1 || !can_run(*e, op, n, nrhs, dev)) continue;
+        if (!best || e->cap < best->cap || (e->cap == best->cap && e->family > best->family) ||
+            (e->cap == best->cap && e->family == best->family && e->p > best->p))
+            best = e;
     }
     if (!best)
         for (const KernelEntry *e : cands)

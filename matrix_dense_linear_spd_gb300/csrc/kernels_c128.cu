@@ -1,10 +1,17 @@
-// Compiled kernel variants for c128 (cf64): register-tile geometries (P, S) and blocked
+// Compiled kernel variants for c128 (cf64): lane-row geometries (P, R), register-tile geometries (P, S)
+// and blocked
 // panel widths. The dispatcher picks among them; see dispatch.cpp.
 #include "launch.cuh"
 
 namespace bl {
 
 static const KernelEntry k_entries_c128[] = {
+    warp_entry<cf64, 4, 2>(),
+    warp_entry<cf64, 8, 1>(),
+    warp_entry<cf64, 8, 2>(),
+    warp_entry<cf64, 16, 1>(),
+    warp_entry<cf64, 16, 2>(),
+    warp_entry<cf64, 32, 1>(),
     tile_entry<cf64, 2, 2>(),
     tile_entry<cf64, 2, 4>(),
     tile_entry<cf64, 4, 3>(),

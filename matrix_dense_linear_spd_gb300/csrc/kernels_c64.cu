@@ -1,10 +1,19 @@
-// Compiled kernel variants for c64 (cf32): register-tile geometries (P, S) and blocked
+// Compiled kernel variants for c64 (cf32): lane-row geometries (P, R), register-tile geometries (P, S)
+// and blocked
 // panel widths. The dispatcher picks among them; see dispatch.cpp.
 #include "launch.cuh"
 
 namespace bl {
 
 static const KernelEntry k_entries_c64[] = {
+    warp_entry<cf32, 4, 2>(),
+    warp_entry<cf32, 8, 1>(),
+    warp_entry<cf32, 4, 4>(),
+    warp_entry<cf32, 8, 2>(),
+    warp_entry<cf32, 16, 1>(),
+    warp_entry<cf32, 8, 3>(),
+    warp_entry<cf32, 16, 2>(),
+    warp_entry<cf32, 32, 1>(),
     tile_entry<cf32, 2, 2>(),
     tile_entry<cf32, 2, 4>(),
     tile_entry<cf32, 4, 3>(),

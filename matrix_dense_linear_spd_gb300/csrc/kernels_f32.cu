@@ -1,10 +1,21 @@
-// Compiled kernel variants for f32 (float): register-tile geometries (P, S) and blocked
+// Compiled kernel variants for f32 (float): lane-row geometries (P, R), register-tile geometries (P, S)
+// and blocked
 // panel widths. The dispatcher picks among them; see dispatch.cpp.
 #include "launch.cuh"
 
 namespace bl {
 
 static const KernelEntry k_entries_f32[] = {
+    warp_entry<float, 4, 2>(),
+    warp_entry<float, 8, 1>(),
+    warp_entry<float, 4, 4>(),
+    warp_entry<float, 8, 2>(),
+    warp_entry<float, 16, 1>(),
+    warp_entry<float, 8, 3>(),
+    warp_entry<float, 4, 8>(),
+    warp_entry<float, 8, 4>(),
+    warp_entry<float, 16, 2>(),
+    warp_entry<float, 32, 1>(),
     tile_entry<float, 2, 2>(),
     tile_entry<float, 2, 4>(),
     tile_entry<float, 4, 3>(),

@@ -1,10 +1,20 @@
-// Compiled kernel variants for f64 (double): register-tile geometries (P, S) and blocked
+// Compiled kernel variants for f64 (double): lane-row geometries (P, R), register-tile geometries (P, S)
+// and blocked
 // panel widths. The dispatcher picks among them; see dispatch.cpp.
 #include "launch.cuh"
 
 namespace bl {
 
 static const KernelEntry k_entries_f64[] = {
+    warp_entry<double, 4, 2>(),
+    warp_entry<double, 8, 1>(),
+    warp_entry<double, 4, 4>(),
+    warp_entry<double, 8, 2>(),
+    warp_entry<double, 16, 1>(),
+    warp_entry<double, 8, 3>(),
+    warp_entry<double, 8, 4>(),
+    warp_entry<double, 16, 2>(),
+    warp_entry<double, 32, 1>(),
     tile_entry<double, 2, 2>(),
     tile_entry<double, 2, 4>(),
     tile_entry<double, 4, 3>(),

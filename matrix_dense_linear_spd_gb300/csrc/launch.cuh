@@ -8,6 +8,7 @@
 #include "registry.h"
 #include "blocked_kernel.cuh"
 #include "tile_kernel.cuh"
+#include "warp_kernel.cuh"
 
 namespace bl {
 
@@ -44,6 +45,23 @@ cudaError_t launch_blocked(const BatchArgs &a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     blocked_kernel<T, NB><<<static_cast<unsigned>(a.batch), C::THREADS, C::smem_bytes, st>>>(a);
     return cudaGetLastError();
+}
+
+template <typename T, int P, int R>
+cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
+    using C = WarpCfg<T, P, R>;
+    static std::atomic<unsigned long long> done{0};
+    cudaError_t e = ensure_smem(warp_kernel<T, P, R>, C::smem_bytes, done);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>((a.batch + C::PER_CTA - 1) / C::PER_CTA);
+    warp_kernel<T, P, R><<<grid, C::THREADS, C::smem_bytes, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int P, int R>
+constexpr KernelEntry warp_entry() {
+    using C = WarpCfg<T, P, R>;
+    return KernelEntry{2, P, R, 0, C::N, -1, C::THREADS, C::PER_CTA, C::smem_bytes, &launch_warp<T, P, R>};
 }
 
 template <typename T, int P, int S>

@@ -9,10 +9,11 @@
 namespace bl {
 
 // `cap` is the largest n + rhs-rows-per-pass the variant holds (0: any order); `rhs_max` the
-// right-hand sides one pass solves (0: any).
+// right-hand sides one pass solves (0: any; -1: the variant does not solve).
 struct KernelEntry {
-    int family;          // 0 = tile, 1 = blocked
-    int p, s, nb;        // tile geometry (p, s) or panel width nb
+    int family;          // 0 = tile, 1 = blocked, 2 = warp (potrf only)
+    int p, s, nb;        // tile geometry (p, s), warp geometry (p lanes, s = rows per lane),
+                         // or blocked panel width nb
     int cap;
     int rhs_max;
     int threads, per_cta;

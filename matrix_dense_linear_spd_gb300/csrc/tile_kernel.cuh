@@ -89,6 +89,10 @@ tile_kernel(const BatchArgs args) {
     // this thread's extra (right-hand-side) row, if any: tile row N-1-c lives at s = S-1, p = P-1-c
     const bool xrow = p >= P - nrhs;
     const int xc = P - 1 - p;
+    // staging copy geometry: RT threads walk a column, CT columns at a time
+    constexpr int RT = TPM < 32 ? TPM : 32;
+    constexpr int CT = TPM / RT;
+    const int sr = tl % RT, sc = tl / RT;
 
     T a[S][S];
 #pragma unroll
@@ -105,13 +109,11 @@ tile_kernel(const BatchArgs args) {
         if (c0 >= n) break;
         if (!upper) {
             // columns c0..c0+P-1 of A, rows c..n-1 (lower part only)
-            const int nr = n - c0;
             if (live)
-                for (int idx = tl; idx < P * nr; idx += TPM) {
-                    const int cc = idx / nr;
-                    const int r = c0 + idx - cc * nr;
+                for (int cc = sc; cc < P; cc += CT) {
                     const int c = c0 + cc;
-                    if (c < n && r >= c) stage[cc * LDST + r] = A[static_cast<int64_t>(c) * lda + r];
+                    if (c >= n) break;
+                    for (int r = c + sr; r < n; r += RT) stage[cc * LDST + r] = A[static_cast<int64_t>(c) * lda + r];
                 }
             tile_sync<WS>();
             const int c = c0 + q;
@@ -122,13 +124,11 @@ tile_kernel(const BatchArgs args) {
             }
         } else {
             // rows c0..c0+P-1 of S = columns of A, A rows 0..i (upper part only)
-            const int nk = min(c0 + P, n);
             if (live)
-                for (int idx = tl; idx < P * nk; idx += TPM) {
-                    const int ii = idx / nk;
-                    const int k = idx - ii * nk;
+                for (int ii = sc; ii < P; ii += CT) {
                     const int i = c0 + ii;
-                    if (i < n && k <= i) stage[ii * LDST + k] = A[static_cast<int64_t>(i) * lda + k];
+                    if (i >= n) break;
+                    for (int k = sr; k <= i; k += RT) stage[ii * LDST + k] = A[static_cast<int64_t>(i) * lda + k];
                 }
             tile_sync<WS>();
             const int i = c0 + p;
@@ -268,13 +268,11 @@ tile_kernel(const BatchArgs args) {
                     if (c < n && i < n && (s > b || p >= q)) stage[q * LDST + i] = a[s][b];
                 }
                 tile_sync<WS>();
-                const int nr = n - c0;
                 if (live)
-                    for (int idx = tl; idx < P * nr; idx += TPM) {
-                        const int cc = idx / nr;
-                        const int r = c0 + idx - cc * nr;
+                    for (int cc = sc; cc < P; cc += CT) {
                         const int cg = c0 + cc;
-                        if (cg < n && r >= cg) A[static_cast<int64_t>(cg) * lda + r] = stage[cc * LDST + r];
+                        if (cg >= n) break;
+                        for (int r = cg + sr; r < n; r += RT) A[static_cast<int64_t>(cg) * lda + r] = stage[cc * LDST + r];
                     }
             } else {
                 const int i = c0 + p;
@@ -284,13 +282,11 @@ tile_kernel(const BatchArgs args) {
                     if (i < n && (t < b || q <= p)) stage[p * LDST + k] = conj(a[b][t]);
                 }
                 tile_sync<WS>();
-                const int nk = min(c0 + P, n);
                 if (live)
-                    for (int idx = tl; idx < P * nk; idx += TPM) {
-                        const int ii = idx / nk;
-                        const int k = idx - ii * nk;
+                    for (int ii = sc; ii < P; ii += CT) {
                         const int ig = c0 + ii;
-                        if (ig < n && k <= ig) A[static_cast<int64_t>(ig) * lda + k] = stage[ii * LDST + k];
+                        if (ig >= n) break;
+                        for (int k = sr; k <= ig; k += RT) A[static_cast<int64_t>(ig) * lda + k] = stage[ii * LDST + k];
                     }
             }
             tile_sync<WS>();

@@ -123,13 +123,15 @@ def other_triangle_unchanged(in_buf, out_buf, n, batch, ld, stride, uplo):
     a = synth.from_colmajor(in_buf, n, n, batch, ld, stride)
     b = synth.from_colmajor(out_buf, n, n, batch, ld, stride)
     other = ~tri_mask(n, uplo)
-    same_tri = np.array_equal(a[:, other].view(np.uint8), b[:, other].view(np.uint8))
+    same_tri = np.array_equal(np.ascontiguousarray(a[:, other]).view(np.uint8),
+                              np.ascontiguousarray(b[:, other]).view(np.uint8))
     # gaps between columns / items
     idx = np.zeros(in_buf.size, bool)
     for c in range(n):
         for_items = np.arange(batch)[:, None] * stride + c * ld + np.arange(n)[None, :]
         idx[for_items.ravel()] = True
-    same_gap = np.array_equal(in_buf[~idx].view(np.uint8), out_buf[~idx].view(np.uint8))
+    same_gap = np.array_equal(np.ascontiguousarray(in_buf[~idx]).view(np.uint8),
+                              np.ascontiguousarray(out_buf[~idx]).view(np.uint8))
     return same_tri and same_gap
 
 
