@@ -95,7 +95,13 @@ def test_can_run_is_capacity_only(bl):
                     assert bl.select_debug("potrf", dt, "U", 1000, 0, 7).startswith(sp + " [pin]")
             finally:
                 bl.set_route("potrf", None)
-            if cap:
+            if cap and rhs < 0:   # factor-only variant: a solve pin is an argument error
+                bl.set_route("posv", sp)
+                try:
+                    assert bl.select_debug("posv", dt, "L", 2, 1, 7).startswith("error:")
+                finally:
+                    bl.set_route("posv", None)
+            elif cap:
                 bl.set_route("posv", sp)
                 try:
                     assert bl.select_debug("posv", dt, "L", cap - rhs, 50, 7).startswith(sp)

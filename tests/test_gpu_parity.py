@@ -112,6 +112,8 @@ def test_every_route_pinned_posv_and_potrs(dtype):
     bl = lib()
     rng = np.random.default_rng(5)
     for spelling, cap, rhs in bl.routes(dtype):
+        if rhs < 0:        # factor-only variant
+            continue
         n = (cap - min(rhs, 3)) if cap else 70
         nrhs = 3 if cap == 0 or rhs >= 3 else rhs
         if n < 1:
