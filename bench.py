@@ -309,7 +309,27 @@ def run_ours(args, ws, rank, local):
         msp = timed(posv_once, "L", args.steps, 2, restore_b=True)
         route_p = bl.last_choice()
         bu = potrf_bytes(n, dtype, "U")
+        # vendor reference point: cuSOLVER batched potrf through torch.linalg.cholesky_ex
+        # (out of place: its time includes torch's copy of the input into the output)
+        Acm = work.view(batch, n, n)
+        vend = {}
+        for up in (False, True):
+            for _ in range(3):
+                torch.linalg.cholesky_ex(Acm, upper=up, check_errors=False)
+            vt = []
+            for _ in range(max(10, args.steps // 4)):
+                work.copy_(pristine)
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                torch.linalg.cholesky_ex(Acm, upper=up, check_errors=False)
+                e1.record(stream)
+                vt.append((e0, e1))
+            torch.cuda.synchronize()
+            ms_v = statistics.median(a.elapsed_time(b) for a, b in vt)
+            vend["upper" if up else "lower"] = {"matrices_per_s": batch / (ms_v / 1e3), "ms_per_call": ms_v}
         also = {
+            "cusolver_potrf_via_torch": vend,
             "potrf_upper": {"matrices_per_s": batch / (statistics.mean(msu) / 1e3),
                             "ms_per_call": statistics.mean(msu), "route": route_u,
                             "gbs": bu * batch / (statistics.mean(msu) / 1e3) / 1e9},

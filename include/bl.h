@@ -122,9 +122,9 @@ bl_status bl_set_route(const char *op, const char *spelling);
 int bl_num_routes(bl_dtype dtype);
 const char *bl_route_name(bl_dtype dtype, int i);
 
-/* Capacity of variant i: returns the largest n + (right-hand sides per pass) it holds, 0 for
- * "any order", or -1 when i is out of range; *rhs_per_pass receives the right-hand sides one
- * pass solves (0 = any). */
+/* Capacity of variant i: returns the largest order it holds (for "tile" variants: n plus the
+ * right-hand sides of one pass; for "warp" variants: n), 0 for "any order", or -1 when i is out
+ * of range; *rhs_per_pass receives the right-hand sides one pass solves (0 = any). */
 int bl_route_capacity(bl_dtype dtype, int i, int *rhs_per_pass);
 
 /*

@@ -50,18 +50,25 @@ cudaError_t launch_blocked(const BatchArgs &a, cudaStream_t st) {
 template <typename T, int P, int R>
 cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     using C = WarpCfg<T, P, R>;
-    static std::atomic<unsigned long long> done{0};
-    cudaError_t e = ensure_smem(warp_kernel<T, P, R>, C::smem_bytes, done);
-    if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>((a.batch + C::PER_CTA - 1) / C::PER_CTA);
-    warp_kernel<T, P, R><<<grid, C::THREADS, C::smem_bytes, st>>>(a);
+    if (a.mode == MODE_POTRF) {
+        static std::atomic<unsigned long long> done{0};
+        cudaError_t e = ensure_smem(warp_kernel<T, P, R, false>, C::smem_potrf, done);
+        if (e != cudaSuccess) return e;
+        warp_kernel<T, P, R, false><<<grid, C::THREADS, C::smem_potrf, st>>>(a);
+    } else {
+        static std::atomic<unsigned long long> done{0};
+        cudaError_t e = ensure_smem(warp_kernel<T, P, R, true>, C::smem_solve, done);
+        if (e != cudaSuccess) return e;
+        warp_kernel<T, P, R, true><<<grid, C::THREADS, C::smem_solve, st>>>(a);
+    }
     return cudaGetLastError();
 }
 
 template <typename T, int P, int R>
 constexpr KernelEntry warp_entry() {
     using C = WarpCfg<T, P, R>;
-    return KernelEntry{2, P, R, 0, C::N, -1, C::THREADS, C::PER_CTA, C::smem_bytes, &launch_warp<T, P, R>};
+    return KernelEntry{2, P, R, 0, C::N, C::RHS, C::THREADS, C::PER_CTA, C::smem_solve, &launch_warp<T, P, R>};
 }
 
 template <typename T, int P, int S>
