@@ -47,20 +47,37 @@ cudaError_t launch_blocked(const BatchArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// Persistent grid for the warp family: enough CTAs to fill every SM at the kernel's occupancy,
+// never more than the work needs.
+template <typename K>
+inline unsigned persistent_grid(K kern, int threads, size_t smem, int64_t ctas_needed) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1, sms = sms > 0 ? sms : 1;
+    const int64_t full = static_cast<int64_t>(sms) * per_sm;
+    return static_cast<unsigned>(ctas_needed < full ? ctas_needed : full);
+}
+
 template <typename T, int P, int R>
 cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     using C = WarpCfg<T, P, R>;
-    const unsigned grid = static_cast<unsigned>((a.batch + C::PER_CTA - 1) / C::PER_CTA);
+    const int64_t groups = (a.batch + C::G - 1) / C::G;
+    const int64_t ctas = (groups + C::WARPS - 1) / C::WARPS;
     if (a.mode == MODE_POTRF) {
+        auto kern = warp_kernel<T, P, R, false, C::min_blocks()>;
+        const size_t sm = a.upper ? C::smem_potrf : C::smem_lower;  // Lower needs no staging slab
         static std::atomic<unsigned long long> done{0};
-        cudaError_t e = ensure_smem(warp_kernel<T, P, R, false>, C::smem_potrf, done);
+        cudaError_t e = ensure_smem(kern, C::smem_potrf, done);
         if (e != cudaSuccess) return e;
-        warp_kernel<T, P, R, false><<<grid, C::THREADS, C::smem_potrf, st>>>(a);
+        kern<<<persistent_grid(kern, C::THREADS, sm, ctas), C::THREADS, sm, st>>>(a);
     } else {
+        auto kern = warp_kernel<T, P, R, true, 1>;
         static std::atomic<unsigned long long> done{0};
-        cudaError_t e = ensure_smem(warp_kernel<T, P, R, true>, C::smem_solve, done);
+        cudaError_t e = ensure_smem(kern, C::smem_solve, done);
         if (e != cudaSuccess) return e;
-        warp_kernel<T, P, R, true><<<grid, C::THREADS, C::smem_solve, st>>>(a);
+        kern<<<persistent_grid(kern, C::THREADS, C::smem_solve, ctas), C::THREADS, C::smem_solve, st>>>(a);
     }
     return cudaGetLastError();
 }

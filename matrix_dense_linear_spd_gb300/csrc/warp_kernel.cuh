@@ -7,51 +7,123 @@
 // !(d > 0) (first failure wins, info = j+1), L(j,j) = sqrt(d), L(i,j) = A(i,j)*rsqrt(d),
 // then A(i,k) -= L(i,j)*conj(L(k,j)) for j < k <= i.
 //
-// GB300 layout: lane l of a partition owns rows i = l + P*rho (rho < R), cyclic, so every lane
-// keeps trailing work as the matrix shrinks; with R > 1 one warp instruction advances G
-// matrices. The column L(:,j) is published once per step into a double-buffered per-partition
-// slot in shared memory and read back as 16-byte broadcast loads (one LDS.128 serves four f32
-// entries for all lanes), which costs far fewer instructions than one shuffle per entry.
-// Lower loads/stores are coalesced per column directly from global memory; Upper reads
-// S(i,c) = conj(A(c,i)) through a per-partition staging slab (P columns at a time), so global
-// accesses stay coalesced there too.
+// GB300 layout:
+//  * lane l of a partition owns rows i = l + P*rho (rho < R), cyclic, so every lane keeps
+//    trailing work as the matrix shrinks; with R > 1 one warp instruction advances G matrices;
+//  * the column L(:,j) is published once per step into a double-buffered per-partition slot in
+//    shared memory and read back as 16-byte broadcast loads (one load serves E entries for all
+//    lanes), far fewer instructions than one shuffle per entry;
+//  * warps are persistent: while a warp factors its current group of G matrices, the next
+//    group's referenced triangle is already streaming into a compacted shared-memory slab by
+//    cp.async (16-byte chunks when the layout is 16-byte aligned, element copies otherwise), so
+//    HBM latency overlaps compute and no registers are tied up by loads in flight. The slab
+//    holds, per matrix, only the chunks that intersect the referenced triangle, and its
+//    per-matrix stride is padded so the partitions of a warp read disjoint banks.
 //
 // posv / potrs (same page, "The fused posv tier" and "posv: the backward solve costs a
 // transpose"): up to RHS right-hand sides per pass live in registers next to the rows. The
 // forward solve L*y = b runs inside the column loop (once column j is scaled, y_j = b_j/L(j,j)
 // is broadcast and rows below subtract L(i,j)*y_j). The backward solve L^H*x = y needs row i of
-// L, which only its owner lane holds: each block of P rows is written once into the staging
-// slab (the transpose through shared memory) and the sweep reads conj(L(i,r)) from there.
-// The solve-capable instantiation is separate, so the factor-only kernel keeps its registers.
+// L, which only its owner lane holds: each block of P rows is written once into a staging slab
+// (the transpose through shared memory) and the sweep reads conj(L(i,r)) from there. The
+// solve-capable instantiation is separate, so the factor-only kernel keeps its registers.
 #pragma once
 
 #include "bl_types.cuh"
 
 namespace bl {
 
+__device__ __forceinline__ unsigned smem_addr(const void *p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+template <int BYTES>
+__device__ __forceinline__ void cp_async_elem(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;\n" ::"r"(smem_addr(dst)), "l"(src), "n"(BYTES)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Compacted per-matrix slab for an N x N item, in chunks of E elements (16 bytes).
+//   Lower: column c keeps rows [E*floor(c/E), N)        (the chunks meeting rows >= c)
+//   Upper: column c keeps rows [0, E*ceil((c+1)/E))     (the chunks meeting rows <= c)
+template <int N, int E>
+struct TriSlab {
+    __host__ __device__ static constexpr int lo_first(int c) { return (c / E) * E; }
+    __host__ __device__ static constexpr int lo_len(int c) { return N - lo_first(c); }
+    __host__ __device__ static constexpr int lo_off(int c) {
+        int o = 0;
+        for (int x = 0; x < c; ++x) o += lo_len(x);
+        return o;
+    }
+    __host__ __device__ static constexpr int up_len(int c) { return ((c + E) / E) * E; }
+    __host__ __device__ static constexpr int up_off(int c) {
+        int o = 0;
+        for (int x = 0; x < c; ++x) o += up_len(x);
+        return o;
+    }
+    static constexpr int size = lo_off(N) > up_off(N) ? lo_off(N) : up_off(N);
+};
+
+// Upper slab offset of column i at run time: sum_{x < i} E*ceil((x+1)/E)
+//   = E*(i + E*m*(m-1)/2 + m*r) with m = floor(i/E), r = i - m*E.
+__device__ __forceinline__ int upper_slab_offset(int i, int E) {
+    const int m = i / E, r = i - m * E;
+    return E * (i + E * m * (m - 1) / 2 + m * r);
+}
+
 template <typename T, int P, int R>
 struct WarpCfg {
-    static constexpr int RHS = 8;                    // right-hand sides per solve pass
     static constexpr int N = P * R;
+    // registers (32-bit words) one lane spends on its rows
+    static constexpr int row_words() {
+        int w = 0;
+        for (int r = 0; r < R; ++r) w += (P * r + P) * static_cast<int>(sizeof(T) / 4);
+        return w;
+    }
+    // right-hand sides per solve pass: as many as fit next to the rows without spilling
+    static constexpr int RHS = row_words() <= 48 ? 8 : (row_words() <= 96 ? 4 : 2);
     static constexpr int G = 32 / P;                 // matrices per warp
     static constexpr int WARPS = 4;
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int PER_CTA = G * WARPS;
-    static constexpr int E = 16 / sizeof(T) > 0 ? 16 / sizeof(T) : 1;  // elements per 16 bytes
-    static constexpr int CB = (N + E - 1) / E * E;  // column-buffer length (16-byte multiple)
+    static constexpr int E = 16 / static_cast<int>(sizeof(T));   // elements per 16 bytes
+    static_assert(N % E == 0, "N must be a multiple of the 16-byte chunk");
+    static constexpr int CB = N;                     // column-buffer length
     static constexpr int RB = (RHS + E - 1) / E * E; // broadcast slots for y_j (16-byte multiple)
     static constexpr int CBX = CB + RB;
     static constexpr int LDU = ((N + 1) % 2) ? N + 1 : N + 2;  // staging leading dim (odd)
+    // per-matrix slab stride: >= the slab, a multiple of E, and congruent to P modulo one bank
+    // cycle (128 bytes), so partition g of a warp starts g*P elements into the bank cycle
+    static constexpr int BANKCYC = 128 / static_cast<int>(sizeof(T));
+    static constexpr int slab_stride() {
+        int s = (TriSlab<N, E>::size + E - 1) / E * E;
+        while (((s - P) % BANKCYC + BANKCYC) % BANKCYC != 0) s += E;
+        return s;
+    }
+    static constexpr int MSTRIDE = slab_stride();
     static constexpr int SLOTS = G * WARPS;
+    static constexpr size_t tri_bytes = sizeof(T) * MSTRIDE * SLOTS;
     static constexpr size_t col_bytes = sizeof(T) * 2 * CBX * SLOTS;
     static constexpr size_t stage_bytes = sizeof(T) * P * LDU * SLOTS;
-    static constexpr size_t off_stage = (col_bytes + 15) / 16 * 16;
+    static constexpr size_t off_col = (tri_bytes + 15) / 16 * 16;
+    static constexpr size_t off_stage = off_col + (col_bytes + 15) / 16 * 16;
     static constexpr size_t off_rs = off_stage + (stage_bytes + 15) / 16 * 16;
     static constexpr size_t rs_bytes = sizeof(real_t<T>) * N * SLOTS;
     static constexpr size_t off_x = off_rs + (rs_bytes + 15) / 16 * 16;
     static constexpr size_t x_bytes = sizeof(T) * 2 * RB * SLOTS;
+    static constexpr size_t smem_lower = off_stage;               // Lower potrf: no staging slab
     static constexpr size_t smem_potrf = off_stage + stage_bytes;
     static constexpr size_t smem_solve = off_x + x_bytes;
+    // launch bound for the factor-only kernel: registers held by the rows (32-bit words) plus
+    // about 45 for addresses and temporaries, rounded down to whole CTAs per SM
+    static constexpr int min_blocks() {
+        const int m = 65536 / (THREADS * (row_words() + 45));
+        return m < 1 ? 1 : (m > 8 ? 8 : m);
+    }
 };
 
 template <typename T>
@@ -59,208 +131,303 @@ struct alignas(16) Vec16 {
     T v[16 / sizeof(T)];
 };
 
-template <typename T, int P, int R, bool SOLVE>
-__global__ void __launch_bounds__(128) warp_kernel(const BatchArgs args) {
+// Closed forms of the slab offsets for run-time column indices.
+template <int N, int E>
+__device__ __forceinline__ int lower_slab_offset(int c) {
+    // sum_{x < c} (N - E*floor(x/E)) = c*N - E*(E*m*(m-1)/2 + m*r), m = floor(c/E), r = c - m*E
+    const int m = c / E, r = c - m * E;
+    return c * N - E * (E * m * (m - 1) / 2 + m * r);
+}
+
+// Issue the asynchronous copy of group `grp`'s referenced triangles into the warp's slab.
+// Lanes map to fixed (matrix, 16-byte chunk) pairs and sweep the columns at run time, so the
+// copy costs a handful of registers, not one address per chunk.
+template <typename T, int P, int R>
+__device__ __forceinline__ void warp_prefetch(const BatchArgs &args, T *tri, int64_t grp, int lane, bool vec) {
     using C = WarpCfg<T, P, R>;
+    constexpr int N = C::N, G = C::G, E = C::E, MS = C::MSTRIDE;
+    const int n = args.n;
+    const int64_t lda = args.lda, sa = args.stride_a;
+    const bool upper = args.upper != 0;
+    const T *A0 = static_cast<const T *>(args.A) + grp * G * sa;
+    const int64_t mleft = args.batch - grp * G;            // live matrices in this group
+    if (vec) {
+        constexpr int NQ = N / E;                          // chunks per full column
+        constexpr int CPC = G * NQ;                        // (matrix, chunk) pairs per column
+        constexpr int CPI = CPC >= 32 ? 1 : 32 / CPC;      // columns per sweep step
+        constexpr int ITER = (CPI * CPC + 31) / 32;
+        for (int c0 = 0; c0 < n; c0 += CPI) {
+#pragma unroll
+            for (int it = 0; it < ITER; ++it) {
+                const int t = lane + 32 * it;
+                const int cc = t / CPC, rem = t - cc * CPC;
+                const int gg = rem / NQ, Q = rem - gg * NQ;
+                const int c = c0 + cc;
+                if (t >= CPI * CPC || c >= n || gg >= mleft) continue;
+                int pos;
+                if (!upper) {
+                    const int f = (c / E) * E;             // first kept row of column c
+                    if (Q * E < f || Q * E >= n) continue;
+                    pos = lower_slab_offset<N, E>(c) + Q * E - f;
+                } else {
+                    if (Q * E > c) continue;               // chunks meeting rows 0..c
+                    pos = upper_slab_offset(c, E) + Q * E;
+                }
+                cp_async_16(tri + gg * MS + pos, A0 + gg * sa + c * lda + Q * E);
+            }
+        }
+    } else {
+        // element copies (any alignment): Lower rows c..n-1, Upper rows 0..c of column c
+        constexpr int EPC = G * N;                         // (matrix, row) pairs per column
+        constexpr int ITER = (EPC + 31) / 32;
+        for (int c = 0; c < n; ++c) {
+#pragma unroll
+            for (int it = 0; it < ITER; ++it) {
+                const int t = lane + 32 * it;
+                const int gg = t / N, r = t - gg * N;
+                if (t >= EPC || gg >= mleft || r >= n) continue;
+                int pos;
+                if (!upper) {
+                    if (r < c) continue;
+                    pos = lower_slab_offset<N, E>(c) + r - (c / E) * E;
+                } else {
+                    if (r > c) continue;
+                    pos = upper_slab_offset(c, E) + r;
+                }
+                cp_async_elem<sizeof(T)>(tri + gg * MS + pos, A0 + gg * sa + c * lda + r);
+            }
+        }
+    }
+    cp_async_commit();
+}
+
+template <typename T, int P, int R, bool SOLVE, int MINB>
+__global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
+    using C = WarpCfg<T, P, R>;
+    using L = TriSlab<C::N, C::E>;
     using Rt = real_t<T>;
     constexpr int N = C::N, G = C::G, E = C::E, CB = C::CB, CBX = C::CBX, LDU = C::LDU, RHS = C::RHS;
-    constexpr int RB = C::RB;
+    constexpr int RB = C::RB, MS = C::MSTRIDE;
     extern __shared__ __align__(16) unsigned char smem[];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int g = lane / P;
-    const int l = lane - g * P;
+    const int l_in = lane - g * P;
     const int slot = warp * G + g;
-    const int64_t mat = static_cast<int64_t>(blockIdx.x) * C::PER_CTA + slot;
-    const bool live = mat < args.batch;
     const int n = args.n;
     const bool upper = args.upper != 0;
-    const int64_t lda = args.lda;
-    T *A = static_cast<T *>(args.A) + (live ? mat * args.stride_a : 0);
-    T *colbuf = reinterpret_cast<T *>(smem) + slot * 2 * CBX;
+    const int64_t lda_in = args.lda;
+    T *tri = reinterpret_cast<T *>(smem) + warp * G * MS;       // the warp's slab (G matrices)
+    T *colbuf = reinterpret_cast<T *>(smem + C::off_col) + slot * 2 * CBX;
     T *stage = reinterpret_cast<T *>(smem + C::off_stage) + slot * P * LDU;
     const int mode = SOLVE ? args.mode : MODE_POTRF;
     const bool factor = mode != MODE_POTRS;
     const int nrhs = SOLVE ? min(args.nrhs, RHS) : 0;
-    T *B = SOLVE ? static_cast<T *>(args.B) + (live ? mat * args.stride_b : 0) : nullptr;
     Rt *rsb = SOLVE ? reinterpret_cast<Rt *>(smem + C::off_rs) + slot * N : nullptr;
     T *xsb = SOLVE ? reinterpret_cast<T *>(smem + C::off_x) + slot * 2 * RB : nullptr;
-    // right-hand sides: b[r][c] = B(l + P*r, c)
-    T b[SOLVE ? R : 1][SOLVE ? RHS : 1];
-    if (SOLVE) {
+
+    // 16-byte chunk copies need every column start 16-byte aligned and whole chunks inside n
+    const bool vec = (n % E == 0) && ((lda_in * static_cast<int64_t>(sizeof(T))) % 16 == 0) &&
+                     ((args.stride_a * static_cast<int64_t>(sizeof(T))) % 16 == 0) &&
+                     ((reinterpret_cast<uintptr_t>(args.A) & 15) == 0);
+    const int64_t ngroups = (args.batch + G - 1) / G;
+    const int64_t gstep = static_cast<int64_t>(gridDim.x) * C::WARPS;
+    int64_t grp = static_cast<int64_t>(blockIdx.x) * C::WARPS + warp;
+    if (grp < ngroups) warp_prefetch<T, P, R>(args, tri, grp, lane, vec);
+
+    for (; grp < ngroups; grp += gstep) {
+        // Opaque copies of the lane index and leading dimension: without them the compiler
+        // hoists every per-element address of the loop body out of this loop and keeps them
+        // all live, which doubles the register count and halves occupancy.
+        int l = l_in;
+        int64_t lda = lda_in;
+        asm volatile("" : "+r"(l));
+        asm volatile("" : "+l"(lda));
+        const int64_t mat = grp * G + g;
+        const bool live = mat < args.batch;
+        T a[R][N];
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int c = 0; c < RHS; ++c) {
-                const int i = l + P * r;
-                b[r][c] = (live && c < nrhs && i < n) ? B[static_cast<int64_t>(c) * args.ldb + i] : zero<T>();
-            }
-    }
+            for (int k = 0; k < N; ++k) a[r][k] = zero<T>();
 
-    T a[R][N];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int k = 0; k < N; ++k) a[r][k] = zero<T>();
-
-    // ------------------------------------------------------------------ load
-    if (!upper) {
-#pragma unroll
-        for (int c = 0; c < N; ++c) {
-            if (c >= n) break;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (P * r + P - 1 < c) continue;          // block r has no row >= c
-                const int i = l + P * r;
-                if (live && i < n && i >= c) a[r][c] = A[static_cast<int64_t>(c) * lda + i];
-            }
-        }
-    } else {
-#pragma unroll
-        for (int cb = 0; cb < R; ++cb) {
-            const int c0 = P * cb;
-            if (c0 >= n) break;
-            // columns c0..c0+P-1 of A are rows c0..c0+P-1 of S; stage their upper parts
-            if (live)
-                for (int ii = 0; ii < P; ++ii) {
-                    const int col = c0 + ii;
-                    if (col >= n) break;
-                    for (int r = l; r <= col; r += P) stage[ii * LDU + r] = A[static_cast<int64_t>(col) * lda + r];
-                }
-            __syncwarp();
-            const int i = c0 + l;
-#pragma unroll
-            for (int c = 0; c < P * cb + P; ++c)
-                if (c <= i && i < n) a[cb][c] = conj(stage[l * LDU + c]);
-            __syncwarp();
-        }
-    }
-
-    // ------------------------------------------------------------------ factor
-    int info = 0;
-#pragma unroll
-    for (int j = 0; j < N; ++j) {
-        if (j >= n) break;
-        const int rj = j / P, lj = j - rj * P;
-        const Rt d = __shfl_sync(0xffffffffu, re(a[rj][j]), g * P + lj);
-        T *col = colbuf + (j & 1) * CBX;
-        Rt rs;
-        if (factor) {
-            const bool ok = d > Rt(0);
-            rs = ok ? rsqrt_of(d) : Rt(0);
-            const Rt ljj = ok ? d * rs : d;
-            if (!ok && info == 0) info = j + 1;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (r < rj) continue;
-                T v = a[r][j];
-                if (r == rj) v = (l == lj) ? from_real<T>(ljj) : (l > lj ? scale(v, rs) : v);
-                else v = scale(v, rs);
-                a[r][j] = v;
-                col[l + P * r] = v;
-            }
-        } else {
-            rs = Rt(1) / d;                                  // the factor is given: 1 / L(j,j)
-        }
-        if (SOLVE) {
-            // forward substitution, axpy form: y_j = b_j / L(j,j), then b_i -= L(i,j) y_j (i > j)
-            if (l == lj) {
-#pragma unroll
-                for (int c = 0; c < RHS; ++c) {
-                    b[rj][c] = scale(b[rj][c], rs);
-                    if (c < nrhs) col[CB + c] = b[rj][c];
-                }
-                rsb[j] = rs;
-            }
-        }
+        // -------------------------------------------------------------- pick from the slab
+        cp_async_wait_all();
         __syncwarp();
-        if (SOLVE) {
+        const T *my = tri + g * MS;
+        if (!upper) {
 #pragma unroll
-            for (int q = 0; q < RB / E; ++q) {
-                if (q * E >= nrhs) break;
-                const Vec16<T> yv = reinterpret_cast<const Vec16<T> *>(col + CB)[q];
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const int c = q * E + e;
-                    if (c >= RHS) continue;
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        if (P * r + P - 1 <= j) continue;          // no row > j in block r
-                        const int i = l + P * r;
-                        if (i > j) sub_mul(b[r][c], a[r][j], yv.v[e]);
-                    }
-                }
-            }
-        }
-        if (!factor) continue;
-        // rank-1 update of the trailing rows/columns k > j, 16 bytes of the column at a time
-#pragma unroll
-        for (int q = (j + 1) / E; q < CB / E; ++q) {
-            if (q * E >= n) break;
-            const Vec16<T> ck = reinterpret_cast<const Vec16<T> *>(col)[q];
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                const int k = q * E + e;
-                if (k <= j || k >= N) continue;
+            for (int c = 0; c < N; ++c) {
+                if (c >= n) break;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    if (P * r + P - 1 < k) continue;       // no row >= k in block r
-                    sub_mul_conj(a[r][k], a[r][j], ck.v[e]);
+                    if (P * r + P - 1 < c) continue;          // block r has no row >= c
+                    const int i = l + P * r;
+                    if (live && i >= c && i < n) a[r][c] = my[L::lo_off(c) + i - L::lo_first(c)];
                 }
             }
-        }
-    }
-
-    // ------------------------------------------------------------------ backward solve
-    if (SOLVE) {
-        // L^H x = y, one block of P rows at a time from the bottom: the block's rows of L are
-        // transposed through the staging slab, then x_i is broadcast and rows r < i subtract
-        // conj(L(i,r)) x_i.
+        } else {
 #pragma unroll
-        for (int rb = R - 1; rb >= 0; --rb) {
-            if (P * rb >= n) continue;
-            __syncwarp();
-            {
-                const int i = P * rb + l;
+            for (int r = 0; r < R; ++r) {
+                const int i = l + P * r;
+                const T *rowp = my + upper_slab_offset(i, E);   // column i of A = row i of S
 #pragma unroll
-                for (int k = 0; k < P * rb + P; ++k)
-                    if (k < i) stage[l * LDU + k] = a[rb][k];
-            }
-            __syncwarp();
-            for (int ii = P - 1; ii >= 0; --ii) {
-                const int i = P * rb + ii;
-                if (i >= n) continue;
-                T *xs = xsb + (i & 1) * RB;
-                if (l == ii) {
-                    const Rt ri = rsb[i];
-#pragma unroll
-                    for (int c = 0; c < RHS; ++c) {
-                        b[rb][c] = scale(b[rb][c], ri);
-                        if (c < nrhs) xs[c] = b[rb][c];
-                    }
-                }
-                __syncwarp();
-#pragma unroll
-                for (int r = 0; r <= rb; ++r) {
-                    const int rr = l + P * r;
-                    if (rr < i) {
-                        const T lir = conj(stage[ii * LDU + rr]);
-#pragma unroll
-                        for (int c = 0; c < RHS; ++c)
-                            if (c < nrhs) sub_mul(b[r][c], lir, xs[c]);
-                    }
-                }
+                for (int c = 0; c < P * r + P; ++c)
+                    if (live && c <= i && i < n) a[r][c] = conj(rowp[c]);
             }
         }
         __syncwarp();
-    }
+        if (grp + gstep < ngroups) warp_prefetch<T, P, R>(args, tri, grp + gstep, lane, vec);
 
-    // ------------------------------------------------------------------ store
-    if (SOLVE && !factor) {
-        // solve only: the factor is read-only; a pass after a posv pass skips failed items
-        const bool solved = args.info == nullptr || !live || args.info[mat] == 0;
-        if (live && solved)
+        T *A = static_cast<T *>(args.A) + (live ? mat * args.stride_a : 0);
+        T *B = SOLVE ? static_cast<T *>(args.B) + (live ? mat * args.stride_b : 0) : nullptr;
+        // right-hand sides: b[r][c] = B(l + P*r, c)
+        T b[SOLVE ? R : 1][SOLVE ? RHS : 1];
+        if (SOLVE) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int c = 0; c < RHS; ++c) {
+                    const int i = l + P * r;
+                    b[r][c] = (live && c < nrhs && i < n) ? B[static_cast<int64_t>(c) * args.ldb + i] : zero<T>();
+                }
+        }
+
+        // ------------------------------------------------------------------ factor
+        int info = 0;
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            if (j >= n) break;
+            const int rj = j / P, lj = j - rj * P;
+            const Rt d = __shfl_sync(0xffffffffu, re(a[rj][j]), g * P + lj);
+            T *col = colbuf + (j & 1) * CBX;
+            Rt rs;
+            if (factor) {
+                const bool ok = d > Rt(0);
+                rs = ok ? rsqrt_of(d) : Rt(0);
+                const Rt ljj = ok ? d * rs : d;
+                if (!ok && info == 0) info = j + 1;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (r < rj) continue;
+                    T v = a[r][j];
+                    if (r == rj) v = (l == lj) ? from_real<T>(ljj) : (l > lj ? scale(v, rs) : v);
+                    else v = scale(v, rs);
+                    a[r][j] = v;
+                    col[l + P * r] = v;
+                }
+            } else {
+                rs = Rt(1) / d;                                  // the factor is given: 1 / L(j,j)
+            }
+            if (SOLVE) {
+                // forward substitution, axpy form: y_j = b_j / L(j,j), then b_i -= L(i,j) y_j (i > j)
+                if (l == lj) {
+#pragma unroll
+                    for (int c = 0; c < RHS; ++c) {
+                        b[rj][c] = scale(b[rj][c], rs);
+                        if (c < nrhs) col[CB + c] = b[rj][c];
+                    }
+                    rsb[j] = rs;
+                }
+            }
+            __syncwarp();
+            if (SOLVE) {
+#pragma unroll
+                for (int q = 0; q < RB / E; ++q) {
+                    if (q * E >= nrhs) break;
+                    const Vec16<T> yv = reinterpret_cast<const Vec16<T> *>(col + CB)[q];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const int c = q * E + e;
+                        if (c >= RHS) continue;
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            if (P * r + P - 1 <= j) continue;          // no row > j in block r
+                            const int i = l + P * r;
+                            if (i > j) sub_mul(b[r][c], a[r][j], yv.v[e]);
+                        }
+                    }
+                }
+            }
+            if (!factor) continue;
+            // rank-1 update of the trailing rows/columns k > j, 16 bytes of the column at a time
+#pragma unroll
+            for (int q = (j + 1) / E; q < CB / E; ++q) {
+                if (q * E >= n) break;
+                const Vec16<T> ck = reinterpret_cast<const Vec16<T> *>(col)[q];
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int k = q * E + e;
+                    if (k <= j || k >= N) continue;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        if (P * r + P - 1 < k) continue;       // no row >= k in block r
+                        sub_mul_conj(a[r][k], a[r][j], ck.v[e]);
+                    }
+                }
+            }
+        }
+
+        // ------------------------------------------------------------------ backward solve
+        if (SOLVE) {
+            // L^H x = y, one block of P rows at a time from the bottom: the block's rows of L are
+            // transposed through the staging slab, then x_i is broadcast and rows r < i subtract
+            // conj(L(i,r)) x_i.
+#pragma unroll
+            for (int rb = R - 1; rb >= 0; --rb) {
+                if (P * rb >= n) continue;
+                __syncwarp();
+                {
+                    const int i = P * rb + l;
+#pragma unroll
+                    for (int k = 0; k < P * rb + P; ++k)
+                        if (k < i) stage[l * LDU + k] = a[rb][k];
+                }
+                __syncwarp();
+                for (int ii = P - 1; ii >= 0; --ii) {
+                    const int i = P * rb + ii;
+                    if (i >= n) continue;
+                    T *xs = xsb + (i & 1) * RB;
+                    if (l == ii) {
+                        const Rt ri = rsb[i];
+#pragma unroll
+                        for (int c = 0; c < RHS; ++c) {
+                            b[rb][c] = scale(b[rb][c], ri);
+                            if (c < nrhs) xs[c] = b[rb][c];
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int r = 0; r <= rb; ++r) {
+                        const int rr = l + P * r;
+                        if (rr < i) {
+                            const T lir = conj(stage[ii * LDU + rr]);
+#pragma unroll
+                            for (int c = 0; c < RHS; ++c)
+                                if (c < nrhs) sub_mul(b[r][c], lir, xs[c]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+        }
+
+        // ------------------------------------------------------------------ store
+        if (SOLVE && !factor) {
+            // solve only: the factor is read-only; a pass after a posv pass skips failed items
+            const bool solved = args.info == nullptr || !live || args.info[mat] == 0;
+            if (live && solved)
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int c = 0; c < RHS; ++c) {
+                        const int i = l + P * r;
+                        if (c < nrhs && i < n) B[static_cast<int64_t>(c) * args.ldb + i] = b[r][c];
+                    }
+            continue;
+        }
+        if (SOLVE && info == 0 && live) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -268,49 +435,51 @@ __global__ void __launch_bounds__(128) warp_kernel(const BatchArgs args) {
                     const int i = l + P * r;
                     if (c < nrhs && i < n) B[static_cast<int64_t>(c) * args.ldb + i] = b[r][c];
                 }
-        return;
-    }
-    if (SOLVE && info == 0 && live) {
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int c = 0; c < RHS; ++c) {
-                const int i = l + P * r;
-                if (c < nrhs && i < n) B[static_cast<int64_t>(c) * args.ldb + i] = b[r][c];
-            }
-    }
-    if (!upper) {
-#pragma unroll
-        for (int c = 0; c < N; ++c) {
-            if (c >= n) break;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (P * r + P - 1 < c) continue;
-                const int i = l + P * r;
-                if (live && i < n && i >= c) A[static_cast<int64_t>(c) * lda + i] = a[r][c];
-            }
         }
-    } else {
-        __syncwarp();
+        // fresh opaque copies again, so the store's per-element predicates are not carried
+        // (as live registers) all the way from the pick above
+        asm volatile("" : "+r"(l));
+        asm volatile("" : "+l"(lda));
+        if (!upper) {
 #pragma unroll
-        for (int cb = 0; cb < R; ++cb) {
-            const int c0 = P * cb;
-            if (c0 >= n) break;
-            const int i = c0 + l;
+            for (int c = 0; c < N; ++c) {
+                if (c >= n) break;
 #pragma unroll
-            for (int c = 0; c < P * cb + P; ++c)
-                if (c <= i && i < n) stage[l * LDU + c] = conj(a[cb][c]);
-            __syncwarp();
-            if (live)
-                for (int ii = 0; ii < P; ++ii) {
-                    const int colx = c0 + ii;
-                    if (colx >= n) break;
-                    for (int r = l; r <= colx; r += P) A[static_cast<int64_t>(colx) * lda + r] = stage[ii * LDU + r];
+                for (int r = 0; r < R; ++r) {
+                    if (P * r + P - 1 < c) continue;
+                    const int i = l + P * r;
+                    if (live && i < n && i >= c) A[static_cast<int64_t>(c) * lda + i] = a[r][c];
                 }
+            }
+        } else {
             __syncwarp();
+#pragma unroll
+            for (int cb = 0; cb < R; ++cb) {
+                const int c0 = P * cb;
+                if (c0 >= n) break;
+                const int i = c0 + l;
+#pragma unroll
+                for (int c = 0; c < P * cb + P; ++c)
+                    if (c <= i && i < n) stage[l * LDU + c] = conj(a[cb][c]);
+                __syncwarp();
+                // U(r, colx) = conj(L(colx, r)) for r <= colx: column colx of U, rows by lane
+                if (live) {
+#pragma unroll
+                    for (int ii = 0; ii < P; ++ii) {
+                        const int colx = c0 + ii;
+#pragma unroll
+                        for (int t = 0; t <= cb; ++t) {
+                            const int r = l + P * t;
+                            if (colx < n && r <= colx) A[static_cast<int64_t>(colx) * lda + r] = stage[ii * LDU + r];
+                        }
+                    }
+                }
+                __syncwarp();
+            }
         }
+        if (live && l == 0) args.info[mat] = info;
     }
-    if (live && l == 0) args.info[mat] = info;
+    cp_async_wait_all();
 }
 
 }  // namespace bl
