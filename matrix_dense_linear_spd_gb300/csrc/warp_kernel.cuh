@@ -95,6 +95,16 @@ struct WarpCfg {
     static constexpr int CB = N;                     // column-buffer length
     static constexpr int RB = (RHS + E - 1) / E * E; // broadcast slots for y_j (16-byte multiple)
     static constexpr int CBX = CB + RB;
+    // per-partition column slots (two buffers): stride congruent to P modulo the bank cycle, so
+    // the partitions of a warp store their columns into disjoint banks
+    static constexpr int col_stride() {
+        int s = 2 * CBX;
+        while (((s - P) % (128 / static_cast<int>(sizeof(T))) + 128 / static_cast<int>(sizeof(T))) %
+                   (128 / static_cast<int>(sizeof(T))) != 0)
+            s += E;
+        return s;
+    }
+    static constexpr int COLS = col_stride();
     static constexpr int LDU = ((N + 1) % 2) ? N + 1 : N + 2;  // staging leading dim (odd)
     // per-matrix slab stride: >= the slab, a multiple of E, and congruent to P modulo one bank
     // cycle (128 bytes), so partition g of a warp starts g*P elements into the bank cycle
@@ -107,7 +117,7 @@ struct WarpCfg {
     static constexpr int MSTRIDE = slab_stride();
     static constexpr int SLOTS = G * WARPS;
     static constexpr size_t tri_bytes = sizeof(T) * MSTRIDE * SLOTS;
-    static constexpr size_t col_bytes = sizeof(T) * 2 * CBX * SLOTS;
+    static constexpr size_t col_bytes = sizeof(T) * COLS * SLOTS;
     static constexpr size_t stage_bytes = sizeof(T) * P * LDU * SLOTS;
     static constexpr size_t off_col = (tri_bytes + 15) / 16 * 16;
     static constexpr size_t off_stage = off_col + (col_bytes + 15) / 16 * 16;
@@ -219,13 +229,35 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
     const bool upper = args.upper != 0;
     const int64_t lda_in = args.lda;
     T *tri = reinterpret_cast<T *>(smem) + warp * G * MS;       // the warp's slab (G matrices)
-    T *colbuf = reinterpret_cast<T *>(smem + C::off_col) + slot * 2 * CBX;
+    T *colbuf = reinterpret_cast<T *>(smem + C::off_col) + slot * C::COLS;
     T *stage = reinterpret_cast<T *>(smem + C::off_stage) + slot * P * LDU;
     const int mode = SOLVE ? args.mode : MODE_POTRF;
     const bool factor = mode != MODE_POTRS;
     const int nrhs = SOLVE ? min(args.nrhs, RHS) : 0;
     Rt *rsb = SOLVE ? reinterpret_cast<Rt *>(smem + C::off_rs) + slot * N : nullptr;
     T *xsb = SOLVE ? reinterpret_cast<T *>(smem + C::off_x) + slot * 2 * RB : nullptr;
+
+    // Identity padding: the slab positions of rows/columns >= n are never written by a prefetch,
+    // so filling the whole slab with the identity once makes every later pick see an n x n item
+    // bordered by the identity. The column loop then runs all N steps with no run-time bounds:
+    // padding pivots are exactly 1 and padding entries stay 0.
+    for (int t = lane; t < G * MS; t += 32) {
+        const int gg = t / MS, e = t - gg * MS;
+        (void)gg;
+        bool diag = false;
+        if (!upper) {
+            // Lower slab: column c at lo_off(c), row i = lo_first(c) + offset
+            int c = 0;
+            while (c + 1 < N && L::lo_off(c + 1) <= e) ++c;
+            diag = (e < L::lo_off(N)) && (L::lo_first(c) + (e - L::lo_off(c)) == c);
+        } else {
+            int c = 0;
+            while (c + 1 < N && L::up_off(c + 1) <= e) ++c;
+            diag = (e < L::up_off(N)) && (e - L::up_off(c) == c);
+        }
+        tri[t] = diag ? from_real<T>(Rt(1)) : zero<T>();
+    }
+    __syncwarp();
 
     // 16-byte chunk copies need every column start 16-byte aligned and whole chunks inside n
     const bool vec = (n % E == 0) && ((lda_in * static_cast<int64_t>(sizeof(T))) % 16 == 0) &&
@@ -246,35 +278,29 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
         asm volatile("" : "+l"(lda));
         const int64_t mat = grp * G + g;
         const bool live = mat < args.batch;
-        T a[R][N];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int k = 0; k < N; ++k) a[r][k] = zero<T>();
 
         // -------------------------------------------------------------- pick from the slab
+        T a[R][N];
         cp_async_wait_all();
         __syncwarp();
         const T *my = tri + g * MS;
         if (!upper) {
 #pragma unroll
-            for (int c = 0; c < N; ++c) {
-                if (c >= n) break;
+            for (int c = 0; c < N; ++c)
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (P * r + P - 1 < c) continue;          // block r has no row >= c
-                    const int i = l + P * r;
-                    if (live && i >= c && i < n) a[r][c] = my[L::lo_off(c) + i - L::lo_first(c)];
+                    // rows i < c of the block read other entries of the slab: they land in the
+                    // unused upper part of the lane's register row and never reach the factor
+                    a[r][c] = my[L::lo_off(c) + l + P * r - L::lo_first(c)];
                 }
-            }
         } else {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int i = l + P * r;
                 const T *rowp = my + upper_slab_offset(i, E);   // column i of A = row i of S
 #pragma unroll
-                for (int c = 0; c < P * r + P; ++c)
-                    if (live && c <= i && i < n) a[r][c] = conj(rowp[c]);
+                for (int c = 0; c < P * r + P; ++c) a[r][c] = conj(rowp[c]);
             }
         }
         __syncwarp();
@@ -282,7 +308,7 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
 
         T *A = static_cast<T *>(args.A) + (live ? mat * args.stride_a : 0);
         T *B = SOLVE ? static_cast<T *>(args.B) + (live ? mat * args.stride_b : 0) : nullptr;
-        // right-hand sides: b[r][c] = B(l + P*r, c)
+        // right-hand sides: b[r][c] = B(l + P*r, c), zero in the padding rows
         T b[SOLVE ? R : 1][SOLVE ? RHS : 1];
         if (SOLVE) {
 #pragma unroll
@@ -294,10 +320,12 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
                 }
         }
 
-        // ------------------------------------------------------------------ factor
-        int info = 0;
+        // -------------------------------------------------------------- factor (+ forward solve)
+        unsigned failed = 0;                                   // bit j: pivot j was not positive
 #pragma unroll
         for (int j = 0; j < N; ++j) {
+            // columns >= n are identity padding: skipping them is exact, and the uniform branch
+            // keeps the scheduler from interleaving all N unrolled steps (which costs registers)
             if (j >= n) break;
             const int rj = j / P, lj = j - rj * P;
             const Rt d = __shfl_sync(0xffffffffu, re(a[rj][j]), g * P + lj);
@@ -307,26 +335,27 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
                 const bool ok = d > Rt(0);
                 rs = ok ? rsqrt_of(d) : Rt(0);
                 const Rt ljj = ok ? d * rs : d;
-                if (!ok && info == 0) info = j + 1;
+                failed |= ok ? 0u : (1u << j);
+                // scale rows >= j (rows < j of block rj are unused upper entries: scaling them
+                // is harmless), then put the diagonal
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (r < rj) continue;
-                    T v = a[r][j];
-                    if (r == rj) v = (l == lj) ? from_real<T>(ljj) : (l > lj ? scale(v, rs) : v);
-                    else v = scale(v, rs);
+                    T v = scale(a[r][j], rs);
+                    if (r == rj && l == lj) v = from_real<T>(ljj);
                     a[r][j] = v;
                     col[l + P * r] = v;
                 }
             } else {
-                rs = Rt(1) / d;                                  // the factor is given: 1 / L(j,j)
+                rs = Rt(1) / d;                                // the factor is given: 1 / L(j,j)
             }
             if (SOLVE) {
-                // forward substitution, axpy form: y_j = b_j / L(j,j), then b_i -= L(i,j) y_j (i > j)
+                // forward substitution, axpy form: y_j = b_j / L(j,j), then b_i -= L(i,j) y_j
                 if (l == lj) {
 #pragma unroll
                     for (int c = 0; c < RHS; ++c) {
                         b[rj][c] = scale(b[rj][c], rs);
-                        if (c < nrhs) col[CB + c] = b[rj][c];
+                        col[CB + c] = b[rj][c];
                     }
                     rsb[j] = rs;
                 }
@@ -335,7 +364,6 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
             if (SOLVE) {
 #pragma unroll
                 for (int q = 0; q < RB / E; ++q) {
-                    if (q * E >= nrhs) break;
                     const Vec16<T> yv = reinterpret_cast<const Vec16<T> *>(col + CB)[q];
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
@@ -343,7 +371,7 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
                         if (c >= RHS) continue;
 #pragma unroll
                         for (int r = 0; r < R; ++r) {
-                            if (P * r + P - 1 <= j) continue;          // no row > j in block r
+                            if (P * r + P - 1 <= j) continue;      // no row > j in block r
                             const int i = l + P * r;
                             if (i > j) sub_mul(b[r][c], a[r][j], yv.v[e]);
                         }
@@ -354,29 +382,28 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
             // rank-1 update of the trailing rows/columns k > j, 16 bytes of the column at a time
 #pragma unroll
             for (int q = (j + 1) / E; q < CB / E; ++q) {
-                if (q * E >= n) break;
                 const Vec16<T> ck = reinterpret_cast<const Vec16<T> *>(col)[q];
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                     const int k = q * E + e;
-                    if (k <= j || k >= N) continue;
+                    if (k <= j) continue;
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        if (P * r + P - 1 < k) continue;       // no row >= k in block r
+                        if (P * r + P - 1 < k) continue;   // no row >= k in block r
                         sub_mul_conj(a[r][k], a[r][j], ck.v[e]);
                     }
                 }
             }
         }
+        const int info = failed ? (__ffs(failed)) : 0;         // first failing column, 1-based
 
-        // ------------------------------------------------------------------ backward solve
+        // -------------------------------------------------------------- backward solve
         if (SOLVE) {
             // L^H x = y, one block of P rows at a time from the bottom: the block's rows of L are
             // transposed through the staging slab, then x_i is broadcast and rows r < i subtract
-            // conj(L(i,r)) x_i.
+            // conj(L(i,r)) x_i. Padding rows carry y = 0, so they contribute nothing.
 #pragma unroll
             for (int rb = R - 1; rb >= 0; --rb) {
-                if (P * rb >= n) continue;
                 __syncwarp();
                 {
                     const int i = P * rb + l;
@@ -387,14 +414,13 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
                 __syncwarp();
                 for (int ii = P - 1; ii >= 0; --ii) {
                     const int i = P * rb + ii;
-                    if (i >= n) continue;
                     T *xs = xsb + (i & 1) * RB;
                     if (l == ii) {
                         const Rt ri = rsb[i];
 #pragma unroll
                         for (int c = 0; c < RHS; ++c) {
                             b[rb][c] = scale(b[rb][c], ri);
-                            if (c < nrhs) xs[c] = b[rb][c];
+                            xs[c] = b[rb][c];
                         }
                     }
                     __syncwarp();
@@ -404,8 +430,7 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
                         if (rr < i) {
                             const T lir = conj(stage[ii * LDU + rr]);
 #pragma unroll
-                            for (int c = 0; c < RHS; ++c)
-                                if (c < nrhs) sub_mul(b[r][c], lir, xs[c]);
+                            for (int c = 0; c < RHS; ++c) sub_mul(b[r][c], lir, xs[c]);
                         }
                     }
                 }
@@ -413,7 +438,11 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
             __syncwarp();
         }
 
-        // ------------------------------------------------------------------ store
+        // -------------------------------------------------------------- store
+        // fresh opaque copies again, so the store's per-element predicates are not carried
+        // (as live registers) all the way from the pick above
+        asm volatile("" : "+r"(l));
+        asm volatile("" : "+l"(lda));
         if (SOLVE && !factor) {
             // solve only: the factor is read-only; a pass after a posv pass skips failed items
             const bool solved = args.info == nullptr || !live || args.info[mat] == 0;
@@ -436,31 +465,30 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
                     if (c < nrhs && i < n) B[static_cast<int64_t>(c) * args.ldb + i] = b[r][c];
                 }
         }
-        // fresh opaque copies again, so the store's per-element predicates are not carried
-        // (as live registers) all the way from the pick above
-        asm volatile("" : "+r"(l));
-        asm volatile("" : "+l"(lda));
         if (!upper) {
+            bool row_ok[R];
 #pragma unroll
-            for (int c = 0; c < N; ++c) {
-                if (c >= n) break;
+            for (int r = 0; r < R; ++r) row_ok[r] = live && (l + P * r < n);
+#pragma unroll
+            for (int c = 0; c < N; ++c)
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (P * r + P - 1 < c) continue;
                     const int i = l + P * r;
-                    if (live && i < n && i >= c) A[static_cast<int64_t>(c) * lda + i] = a[r][c];
+                    if (row_ok[r] && i >= c) A[static_cast<int64_t>(c) * lda + i] = a[r][c];
                 }
-            }
         } else {
-            __syncwarp();
+            // U(c,i) = conj(L(i,c)): column i of U is row i of L; transpose through the slab,
+            // one block of P rows (= P columns of U) at a time
 #pragma unroll
             for (int cb = 0; cb < R; ++cb) {
                 const int c0 = P * cb;
                 if (c0 >= n) break;
+                __syncwarp();
                 const int i = c0 + l;
 #pragma unroll
                 for (int c = 0; c < P * cb + P; ++c)
-                    if (c <= i && i < n) stage[l * LDU + c] = conj(a[cb][c]);
+                    if (c <= i) stage[l * LDU + c] = conj(a[cb][c]);
                 __syncwarp();
                 // U(r, colx) = conj(L(colx, r)) for r <= colx: column colx of U, rows by lane
                 if (live) {
@@ -474,7 +502,6 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
                         }
                     }
                 }
-                __syncwarp();
             }
         }
         if (live && l == 0) args.info[mat] = info;

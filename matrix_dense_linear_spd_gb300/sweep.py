@@ -141,7 +141,18 @@ def main(argv=None):
     dev = torch.cuda.get_device_properties(0)
     devkey = f"sm_{dev.major}{dev.minor}"
     l2 = dev.L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+    # evict L2 between reps: write one buffer larger than L2, then read another, so L2 is left
+    # clean and no write-back of the flush lands inside a timed call
+    fa = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device="cuda")
+    fb = torch.ones_like(fa)
+    sink = torch.empty((), dtype=torch.float32, device="cuda")
+
+    class _Flush:
+        @staticmethod
+        def zero_():
+            fa.zero_()
+            torch.sum(fb, dim=0, out=sink)
+    flush = _Flush()
     ns = [int(x) for x in a.n.split(",")] if a.n else (POTRF_N if a.op == "potrf" else POSV_N)
     nrhss = [int(x) for x in a.nrhs.split(",")] if a.op == "posv" else [0]
     ledger = open(os.path.join(a.out, f"{a.op}.{devkey}.jsonl"), "a")
