@@ -241,21 +241,12 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
     // so filling the whole slab with the identity once makes every later pick see an n x n item
     // bordered by the identity. The column loop then runs all N steps with no run-time bounds:
     // padding pivots are exactly 1 and padding entries stay 0.
-    for (int t = lane; t < G * MS; t += 32) {
-        const int gg = t / MS, e = t - gg * MS;
-        (void)gg;
-        bool diag = false;
-        if (!upper) {
-            // Lower slab: column c at lo_off(c), row i = lo_first(c) + offset
-            int c = 0;
-            while (c + 1 < N && L::lo_off(c + 1) <= e) ++c;
-            diag = (e < L::lo_off(N)) && (L::lo_first(c) + (e - L::lo_off(c)) == c);
-        } else {
-            int c = 0;
-            while (c + 1 < N && L::up_off(c + 1) <= e) ++c;
-            diag = (e < L::up_off(N)) && (e - L::up_off(c) == c);
-        }
-        tri[t] = diag ? from_real<T>(Rt(1)) : zero<T>();
+    for (int t = lane; t < G * MS; t += 32) tri[t] = zero<T>();
+    __syncwarp();
+    for (int t = lane; t < G * N; t += 32) {
+        const int gg = t / N, c = t - gg * N;
+        const int pos = upper ? upper_slab_offset(c, E) + c : lower_slab_offset<N, E>(c) + c - (c / E) * E;
+        tri[gg * MS + pos] = from_real<T>(Rt(1));
     }
     __syncwarp();
 
