@@ -6,7 +6,6 @@
 #pragma once
 
 #include <cstdint>
-#include <type_traits>
 #include <cuda_runtime.h>
 
 namespace bl {
@@ -87,18 +86,6 @@ __device__ __forceinline__ void add_into(float &a, float b) { a += b; }
 __device__ __forceinline__ void add_into(double &a, double b) { a += b; }
 __device__ __forceinline__ void add_into(cf32 &a, cf32 b) { a.x += b.x; a.y += b.y; }
 __device__ __forceinline__ void add_into(cf64 &a, cf64 b) { a.x += b.x; a.y += b.y; }
-
-// (acc0, acc1) += m * (v0, v1) as one packed two-lane FP32 FMA (sm_100+ fma.rn.f32x2).
-__device__ __forceinline__ void fma2(float &acc0, float &acc1, float m, float v0, float v1) {
-    asm("{\n\t.reg .b64 a, x, y;\n\t"
-        "mov.b64 a, {%0, %1};\n\t"
-        "mov.b64 x, {%2, %2};\n\t"
-        "mov.b64 y, {%3, %4};\n\t"
-        "fma.rn.f32x2 a, x, y, a;\n\t"
-        "mov.b64 {%0, %1}, a;\n\t}"
-        : "+f"(acc0), "+f"(acc1)
-        : "f"(m), "f"(v0), "f"(v1));
-}
 
 __device__ __forceinline__ float rsqrt_of(float d) { return rsqrtf(d); }
 __device__ __forceinline__ double rsqrt_of(double d) { return rsqrt(d); }

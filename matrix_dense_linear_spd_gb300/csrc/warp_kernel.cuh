@@ -218,7 +218,6 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
     using Rt = real_t<T>;
     constexpr int N = C::N, G = C::G, E = C::E, CB = C::CB, CBX = C::CBX, LDU = C::LDU, RHS = C::RHS;
     constexpr int RB = C::RB, MS = C::MSTRIDE;
-    constexpr bool kPacked = std::is_same<T, float>::value;   // packed two-lane FP32 FMA
     extern __shared__ __align__(16) unsigned char smem[];
 
     const int lane = threadIdx.x & 31;
@@ -336,8 +335,7 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
                     T v = scale(a[r][j], rs);
                     if (r == rj && l == lj) v = from_real<T>(ljj);
                     a[r][j] = v;
-                    // f32 publishes -L(i,j) so the update is a plain packed FMA
-                    col[l + P * r] = kPacked ? scale(v, Rt(-1)) : v;
+                    col[l + P * r] = v;
                 }
             } else {
                 rs = Rt(1) / d;                                // the factor is given: 1 / L(j,j)
@@ -376,31 +374,14 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
 #pragma unroll
             for (int q = (j + 1) / E; q < CB / E; ++q) {
                 const Vec16<T> ck = reinterpret_cast<const Vec16<T> *>(col)[q];
-                if constexpr (kPacked) {
-                    // pairs of columns (k, k+1) in one fma.rn.f32x2: a(i,k) += L(i,j) * (-L(k,j))
 #pragma unroll
-                    for (int e = 0; e < E; e += 2) {
-                        const int k = q * E + e;
-                        if (k + 1 <= j) continue;
+                for (int e = 0; e < E; ++e) {
+                    const int k = q * E + e;
+                    if (k <= j) continue;
 #pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            if (P * r + P - 1 < k) continue;
-                            if (k <= j)
-                                a[r][k + 1] = fmaf(a[r][j], ck.v[e + 1], a[r][k + 1]);
-                            else
-                                fma2(a[r][k], a[r][k + 1], a[r][j], ck.v[e], ck.v[e + 1]);
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const int k = q * E + e;
-                        if (k <= j) continue;
-#pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            if (P * r + P - 1 < k) continue;   // no row >= k in block r
-                            sub_mul_conj(a[r][k], a[r][j], ck.v[e]);
-                        }
+                    for (int r = 0; r < R; ++r) {
+                        if (P * r + P - 1 < k) continue;   // no row >= k in block r
+                        sub_mul_conj(a[r][k], a[r][j], ck.v[e]);
                     }
                 }
             }
