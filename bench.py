@@ -205,6 +205,20 @@ def recorded_traffic(kernel_tag: str):
     return e.get("dram_bytes_per_launch")
 
 
+def aggregate(ms_local: float, batch: int, dist=None, device=None):
+    """Weak-scaling aggregate over ranks: every rank factors its own batch, the job time is the
+    slowest rank's, and the value counts the matrices of all ranks. Returns (ms_max, value)."""
+    import torch
+    ms_max = ms_local
+    ws = 1
+    if dist is not None and dist.is_initialized():
+        ws = dist.get_world_size()
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    return ms_max, ws * batch / (ms_max / 1e3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -313,13 +327,8 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     sampler.stop()
     ms_step = sum(ms) / len(ms)
-    ms_max = ms_step
-    if dist:
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_max = float(tt.item())
+    ms_max, value = aggregate(ms_step, batch, dist, dev)
     ok_info = int(info.abs().sum().item()) == 0
-    value = ws * batch / (ms_max / 1e3)
 
     # extras on the same batch: Upper potrf and posv
     also = {}
@@ -375,11 +384,7 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         if it >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_step = statistics.mean(e2e_ms)
-    if dist:
-        tt = torch.tensor([e2e_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_step = float(tt.item())
+    e2e_step, _ = aggregate(statistics.mean(e2e_ms), batch, dist, dev)
 
     peaks, peak_src = measured_peaks()
     alg_bytes = potrf_bytes(n, dtype, "L") * batch

@@ -137,6 +137,16 @@ int bl_route_capacity(bl_dtype dtype, int i, int *rhs_per_pass);
 const char *bl_select_debug(int op, bl_dtype dtype, bl_uplo uplo, int64_t n, int64_t nrhs,
                             int64_t batch, const char *devkey, int64_t smem_optin);
 
+/*
+ * Diagnostic: one 128 x 128 tile C = A * B^T on the tensor cores (tcgen05, kind::tf32) with the
+ * 3xTF32 split the blocked factorisation's trailing update uses. A and B are device pointers to
+ * 128 x 32 row-major f32 matrices, C to a 128 x 128 row-major f32 result; *status (device int32,
+ * initially 0) becomes 1 on completion or 2 if the tensor-core work did not complete within the
+ * kernel's bounded wait. Launches one CTA on `stream`.
+ */
+bl_status bl_debug_tc_tile_f32(const float *A, const float *B, float *C, int32_t *status,
+                               bl_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ STATUS = {0: "success", 1: "invalid argument", 2: "no route", 3: "CUDA error", 4
 
 EXPORTED = ("bl_potrf", "bl_posv", "bl_potrs", "bl_status_string", "bl_last_error", "bl_last_choice",
             "bl_version", "bl_set_route", "bl_num_routes", "bl_route_name", "bl_route_capacity",
-            "bl_select_debug")
+            "bl_select_debug", "bl_debug_tc_tile_f32")
 
 
 class BLError(RuntimeError):
@@ -60,6 +60,8 @@ def _load():
     lib.bl_select_debug.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, i64, i64, i64,
                                     ctypes.c_char_p, i64]
     lib.bl_select_debug.restype = ctypes.c_char_p
+    lib.bl_debug_tc_tile_f32.argtypes = [vp, vp, vp, vp, vp]
+    lib.bl_debug_tc_tile_f32.restype = ctypes.c_int
     return lib
 
 

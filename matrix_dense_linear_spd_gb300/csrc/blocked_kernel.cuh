@@ -14,9 +14,17 @@
 // index that is contiguous in memory varies fastest across threads.
 // posv / potrs: after the factor, forward (L*y = b, axpy form) and back (L^H*x = y, axpy form
 // on the rows of L) substitution in global memory ("The fused potrs solve").
+//
+// Tensor-core variant (TC, f32 only): the trailing update -- the only dense contraction of the
+// factorisation -- runs on the fifth-generation tensor cores. Each 128 x 128 lower tile of
+// L21*L21^T is formed in tensor memory by tcgen05.mma kind::tf32 from 128-byte-swizzled
+// K-major operand tiles in shared memory, with the 3xTF32 split (hi*hi + hi*lo + lo*hi, each
+// f32 split into a rounded tf32 part and a tf32 remainder) so the product keeps f32 accuracy;
+// the epilogue reads the tile back with tcgen05.ld and subtracts it from the lower triangle.
 #pragma once
 
 #include "bl_types.cuh"
+#include "tc_sm100.cuh"
 
 namespace bl {
 
@@ -34,8 +42,9 @@ struct SView {  // the Lower view S of the stored matrix
     }
 };
 
-template <typename T, int NB>
+template <typename T, int NB, bool TC = false>
 struct BlkCfg {
+    static_assert(!TC || (NB <= 32 && sizeof(T) == 4), "tensor-core path: f32, panel width <= 32");
     static constexpr int THREADS = 256;
     static constexpr int TB = 64;             // trailing tile edge; 16 x 16 threads x (4 x 4)
     static constexpr int LDD = NB + 1;        // diagonal block leading dimension
@@ -46,16 +55,19 @@ struct BlkCfg {
     static constexpr size_t rs_bytes = sizeof(R) * NB;
     static constexpr size_t panel_bytes = sizeof(T) * THREADS * LDP;
     static constexpr size_t trail_bytes = sizeof(T) * 2 * NB * LDT;
-    static constexpr size_t work_bytes = panel_bytes > trail_bytes ? panel_bytes : trail_bytes;
+    // tensor-core operand tiles: A and B, hi and lo, 128 rows x 128 bytes each, 1024-aligned
+    static constexpr size_t tc_bytes = TC ? 4 * 16384 + 1024 : 0;
+    static constexpr size_t simt_work = panel_bytes > trail_bytes ? panel_bytes : trail_bytes;
+    static constexpr size_t work_bytes = simt_work > tc_bytes ? simt_work : tc_bytes;
     static constexpr size_t off_diag = 0;
     static constexpr size_t off_rs = off_diag + diag_bytes;
     static constexpr size_t off_work = ((off_rs + rs_bytes) + 15) / 16 * 16;
     static constexpr size_t smem_bytes = off_work + work_bytes;
 };
 
-template <typename T, int NB>
+template <typename T, int NB, bool TC = false>
 __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
-    using C = BlkCfg<T, NB>;
+    using C = BlkCfg<T, NB, TC>;
     using R = typename C::R;
     constexpr int THREADS = C::THREADS, TB = C::TB, LDD = C::LDD, LDP = C::LDP, LDT = C::LDT;
     extern __shared__ __align__(16) unsigned char smem[];
@@ -72,7 +84,23 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
     const SView<T> S{static_cast<T *>(args.A) + mat * args.stride_a, args.lda, upper};
     // a solve-only pass that follows a posv pass is given info and skips the failed items
     if (tid == 0) s_fail = (mode == MODE_POTRS && args.info != nullptr && args.info[mat] != 0) ? 1 : 0;
+    // tensor-core resources: 128 tensor-memory columns (one 128 x 128 f32 tile) and an mbarrier
+    __shared__ uint32_t s_tmem;
+    __shared__ uint64_t s_mbar;
+    uint32_t mma_phase = 0;
+    if constexpr (TC) {
+        if ((tid >> 5) == 0) {
+            tc::tmem_alloc(&s_tmem, 128);
+            tc::tmem_relinquish();
+        }
+        if (tid == 0) {
+            tc::mbar_init(&s_mbar, 1);
+            tc::mbar_fence_init();
+        }
+        tc::fence_before_sync();
+    }
     __syncthreads();
+    if constexpr (TC) tc::fence_after_sync();
 
     if (mode != MODE_POTRS) {
         for (int j0 = 0; j0 < n; j0 += NB) {
@@ -144,6 +172,86 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
             // ---------------------------------------------- 3. trailing update (lower tiles)
             const int mt = n - m0;
             if (mt <= 0) continue;
+            if constexpr (TC) {
+                unsigned char *tbase = reinterpret_cast<unsigned char *>(sW);
+                tbase += (1024 - (tc::smem_u32(tbase) & 1023)) & 1023;
+                unsigned char *a_hi = tbase, *a_lo = tbase + 16384, *b_hi = tbase + 32768, *b_lo = tbase + 49152;
+                const uint32_t tmem = s_tmem;
+                const int warp = tid >> 5, lane = tid & 31;
+                const int ntile = (mt + 127) / 128;
+                // operand tile: rows R0..R0+127 of L21 (k < kb), zero-padded, split into tf32 hi/lo
+                auto load_tile = [&](int R0, unsigned char *hi, unsigned char *lo) {
+                    for (int idx = tid; idx < 128 * 32; idx += THREADS) {
+                        const int row = upper ? idx >> 5 : idx & 127;
+                        const int k = upper ? idx & 31 : idx >> 7;
+                        float v = 0.f;
+                        if (R0 + row < n && k < kb) v = S.get(R0 + row, j0 + k);
+                        float h, l;
+                        tc::split_tf32(v, h, l);
+                        const uint32_t off = tc::sw128_offset(row, k);
+                        *reinterpret_cast<float *>(hi + off) = h;
+                        *reinterpret_cast<float *>(lo + off) = l;
+                    }
+                };
+                for (int bi = 0; bi < ntile; ++bi) {
+                    const int I0 = m0 + bi * 128;
+                    load_tile(I0, a_hi, a_lo);
+                    for (int bk = 0; bk <= bi; ++bk) {
+                        const int K0 = m0 + bk * 128;
+                        const bool diag_tile = bk == bi;
+                        if (!diag_tile) load_tile(K0, b_hi, b_lo);
+                        tc::fence_proxy_async_smem();
+                        tc::fence_before_sync();
+                        __syncthreads();
+                        tc::fence_after_sync();
+                        if (tid == 0) {
+                            constexpr uint32_t idesc = tc::idesc_tf32(128, 128);
+                            const uint32_t sa_hi = tc::smem_u32(a_hi), sa_lo = tc::smem_u32(a_lo);
+                            const uint32_t sb_hi = tc::smem_u32(diag_tile ? a_hi : b_hi);
+                            const uint32_t sb_lo = tc::smem_u32(diag_tile ? a_lo : b_lo);
+                            for (int st = 0; st < 4; ++st)
+                                tc::mma_tf32(tmem, tc::sdesc_sw128(sa_hi + 32 * st), tc::sdesc_sw128(sb_hi + 32 * st), idesc,
+                                             st > 0);
+                            for (int st = 0; st < 4; ++st)
+                                tc::mma_tf32(tmem, tc::sdesc_sw128(sa_hi + 32 * st), tc::sdesc_sw128(sb_lo + 32 * st), idesc,
+                                             true);
+                            for (int st = 0; st < 4; ++st)
+                                tc::mma_tf32(tmem, tc::sdesc_sw128(sa_lo + 32 * st), tc::sdesc_sw128(sb_hi + 32 * st), idesc,
+                                             true);
+                            tc::mma_commit(&s_mbar);
+                        }
+                        const bool done = tc::mbar_wait(&s_mbar, mma_phase & 1, 1u << 22);
+                        ++mma_phase;
+                        tc::fence_after_sync();
+                        if (!done) {
+                            // the tensor core did not finish within the bounded wait: report an
+                            // internal error for this item instead of hanging
+                            if (tid == 0) { args.info[mat] = -1; s_fail = 1; }
+                        } else {
+                            // epilogue: TMEM lanes = tile rows (warp w reads lanes 32*(w%4)..), the
+                            // two warp halves take column halves; subtract into the lower triangle
+                            const int row = 32 * (warp & 3) + lane;
+                            const int gi = I0 + row;
+#pragma unroll
+                            for (int cc = 0; cc < 2; ++cc) {
+                                const int c0 = 64 * (warp >> 2) + 32 * cc;
+                                float v[32];
+                                tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + c0, v);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    const int gk = K0 + c0 + i;
+                                    if (gi < n && gk < n && gi >= gk) S.set(gi, gk, S.get(gi, gk) - v[i]);
+                                }
+                            }
+                        }
+                        tc::fence_before_sync();
+                        __syncthreads();
+                        tc::fence_after_sync();
+                    }
+                }
+                if (s_fail) break;
+                continue;
+            }
             const int ntile = (mt + TB - 1) / TB;
             T *sI = sW;
             T *sK = sW + NB * LDT;
@@ -196,6 +304,11 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
         }
         if (tid == 0 && !s_fail) args.info[mat] = 0;
         __syncthreads();
+    }
+    if constexpr (TC) {
+        tc::fence_before_sync();
+        __syncthreads();
+        if ((tid >> 5) == 0) tc::tmem_dealloc(s_tmem, 128);
     }
 
     // ---------------------------------------------- solves (posv after success, potrs)

@@ -75,6 +75,7 @@ std::string spelling(const KernelEntry &e) {
     char buf[64];
     if (e.family == 0) snprintf(buf, sizeof buf, "tile:p=%d:s=%d", e.p, e.s);
     else if (e.family == 2) snprintf(buf, sizeof buf, "warp:p=%d:r=%d", e.p, e.s);
+    else if (e.s) snprintf(buf, sizeof buf, "blocked:nb=%d:tc=1", e.nb);   // tensor-core trailing update
     else snprintf(buf, sizeof buf, "blocked:nb=%d", e.nb);
     return buf;
 }
@@ -93,7 +94,7 @@ std::string canon(std::string s) {
     while (std::getline(ss, tok, ':')) parts.push_back(tok);
     if (parts.empty()) return s;
     static const std::map<std::string, std::vector<std::string>> fields = {
-        {"tile", {"p", "s"}}, {"warp", {"p", "r"}}, {"blocked", {"nb"}}};
+        {"tile", {"p", "s"}}, {"warp", {"p", "r"}}, {"blocked", {"nb", "tc"}}};
     auto it = fields.find(parts[0]);
     if (it == fields.end()) return s;
     std::string out = parts[0];

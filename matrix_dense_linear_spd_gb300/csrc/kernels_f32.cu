@@ -33,6 +33,7 @@ static const KernelEntry k_entries_f32[] = {
     tile_entry<float, 16, 10>(),
     blocked_entry<float, 32>(),
     blocked_entry<float, 64>(),
+    blocked_entry<float, 32, true>(),
 };
 
 const KernelEntry *entries_f32(int *count) {

@@ -37,13 +37,13 @@ cudaError_t launch_tile(const BatchArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <typename T, int NB>
+template <typename T, int NB, bool TC = false>
 cudaError_t launch_blocked(const BatchArgs &a, cudaStream_t st) {
-    using C = BlkCfg<T, NB>;
+    using C = BlkCfg<T, NB, TC>;
     static std::atomic<unsigned long long> done{0};
-    cudaError_t e = ensure_smem(blocked_kernel<T, NB>, C::smem_bytes, done);
+    cudaError_t e = ensure_smem(blocked_kernel<T, NB, TC>, C::smem_bytes, done);
     if (e != cudaSuccess) return e;
-    blocked_kernel<T, NB><<<static_cast<unsigned>(a.batch), C::THREADS, C::smem_bytes, st>>>(a);
+    blocked_kernel<T, NB, TC><<<static_cast<unsigned>(a.batch), C::THREADS, C::smem_bytes, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -94,10 +94,10 @@ constexpr KernelEntry tile_entry() {
     return KernelEntry{0, P, S, 0, C::N, P, C::THREADS, C::G, C::smem_bytes, &launch_tile<T, P, S>};
 }
 
-template <typename T, int NB>
+template <typename T, int NB, bool TC = false>
 constexpr KernelEntry blocked_entry() {
-    using C = BlkCfg<T, NB>;
-    return KernelEntry{1, 0, 0, NB, 0, 0, C::THREADS, 1, C::smem_bytes, &launch_blocked<T, NB>};
+    using C = BlkCfg<T, NB, TC>;
+    return KernelEntry{1, 0, TC ? 1 : 0, NB, 0, 0, C::THREADS, 1, C::smem_bytes, &launch_blocked<T, NB, TC>};
 }
 
 }  // namespace bl

@@ -13,7 +13,7 @@ namespace bl {
 struct KernelEntry {
     int family;          // 0 = tile, 1 = blocked, 2 = warp (potrf only)
     int p, s, nb;        // tile geometry (p, s), warp geometry (p lanes, s = rows per lane),
-                         // or blocked panel width nb
+                         // or blocked panel width nb (s = 1: tensor-core trailing update)
     int cap;
     int rhs_max;
     int threads, per_cta;
