@@ -55,8 +55,11 @@ struct BlkCfg {
     static constexpr size_t rs_bytes = sizeof(R) * NB;
     static constexpr size_t panel_bytes = sizeof(T) * THREADS * LDP;
     static constexpr size_t trail_bytes = sizeof(T) * 2 * NB * LDT;
-    // tensor-core operand tiles: A and B, hi and lo, 128 rows x 128 bytes each, 1024-aligned
-    static constexpr size_t tc_bytes = TC ? 4 * 16384 + 1024 : 0;
+    // tensor-core path: the whole L21 panel stays resident as tf32 hi and lo operand panels
+    // (TC_MAXM rows x 128 bytes each, 128-byte-swizzled K-major), next to the panel staging area
+    static constexpr int TC_MAXM = 512;                        // trailing rows: n <= TC_MAXM + NB
+    static constexpr size_t tc_panel = static_cast<size_t>(TC_MAXM) * 128;
+    static constexpr size_t tc_bytes = TC ? panel_bytes + 1024 + 2 * tc_panel : 0;
     static constexpr size_t simt_work = panel_bytes > trail_bytes ? panel_bytes : trail_bytes;
     static constexpr size_t work_bytes = simt_work > tc_bytes ? simt_work : tc_bytes;
     static constexpr size_t off_diag = 0;
@@ -86,15 +89,16 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
     if (tid == 0) s_fail = (mode == MODE_POTRS && args.info != nullptr && args.info[mat] != 0) ? 1 : 0;
     // tensor-core resources: 128 tensor-memory columns (one 128 x 128 f32 tile) and an mbarrier
     __shared__ uint32_t s_tmem;
-    __shared__ uint64_t s_mbar;
-    uint32_t mma_phase = 0;
+    __shared__ uint64_t s_mbar[2];
+    uint32_t mma_phases = 0;                                   // bit b: parity of accumulator b
     if constexpr (TC) {
         if ((tid >> 5) == 0) {
-            tc::tmem_alloc(&s_tmem, 128);
+            tc::tmem_alloc(&s_tmem, 256);                      // two 128 x 128 f32 accumulators
             tc::tmem_relinquish();
         }
         if (tid == 0) {
-            tc::mbar_init(&s_mbar, 1);
+            tc::mbar_init(&s_mbar[0], 1);
+            tc::mbar_init(&s_mbar[1], 1);
             tc::mbar_fence_init();
         }
         tc::fence_before_sync();
@@ -114,6 +118,38 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
             }
             __syncthreads();
             int fail_col = -1;
+            if constexpr (TC) {
+                // one warp factors the (<= 32) x 32 diagonal block in registers: lane r holds row
+                // r; pivots and column entries travel by shuffles; the other warps wait
+                __shared__ int s_diag_fail;
+                if ((tid >> 5) == 0) {
+                    const int lane = tid & 31;
+                    float a[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) a[c] = (c <= lane && lane < kb) ? sD[c * LDD + lane] : (c == lane ? 1.f : 0.f);
+                    unsigned failed = 0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float d = __shfl_sync(0xffffffffu, a[j], j);
+                        const bool ok = d > 0.f;
+                        const float rs = ok ? rsqrtf(d) : 0.f;
+                        failed |= (ok || j >= kb) ? 0u : (1u << j);
+                        a[j] = (lane == j) ? (ok ? d * rs : d) : (lane > j ? a[j] * rs : a[j]);
+#pragma unroll
+                        for (int k = j + 1; k < 32; ++k) {
+                            const float lk = __shfl_sync(0xffffffffu, a[j], k);
+                            a[k] = fmaf(-a[j], lk, a[k]);
+                        }
+                        if (lane == j) sRs[j] = rs;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (c <= lane && lane < kb) sD[c * LDD + lane] = a[c];
+                    if (lane == 0) s_diag_fail = failed ? __ffs(failed) - 1 : -1;
+                }
+                __syncthreads();
+                fail_col = s_diag_fail;
+            } else
             for (int c = 0; c < kb; ++c) {
                 const R d = re(sD[c * LDD + c]);
                 const bool ok = d > R(0);
@@ -143,6 +179,22 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
             __syncthreads();
             // ---------------------------------------------- 2. panel solve L21 = A21 L11^{-H}
             const int m0 = j0 + kb;
+            const int mt_all = n - m0;
+            unsigned char *p_hi = nullptr, *p_lo = nullptr;
+            if constexpr (TC) {
+                unsigned char *pb = reinterpret_cast<unsigned char *>(sW) + C::panel_bytes;
+                pb += (1024 - (tc::smem_u32(pb) & 1023)) & 1023;
+                p_hi = pb;
+                p_lo = pb + C::tc_panel;
+                // zero the padding rows of the last 128-row operand tile
+                const int mpad = (mt_all + 127) / 128 * 128;
+                for (int idx = tid; idx < (mpad - mt_all) * 32; idx += THREADS) {
+                    const int row = mt_all + (idx >> 5), k = idx & 31;
+                    const uint32_t off = tc::sw128_offset(row, k);
+                    *reinterpret_cast<float *>(p_hi + off) = 0.f;
+                    *reinterpret_cast<float *>(p_lo + off) = 0.f;
+                }
+            }
             for (int rb = m0; rb < n; rb += THREADS) {
                 const int nrow = min(THREADS, n - rb);
                 for (int idx = tid; idx < nrow * kb; idx += THREADS) {
@@ -159,6 +211,17 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
                         for (int m = 0; m < k; ++m) sub_mul_conj(x, row[m], sD[m * LDD + k]);
                         row[k] = scale(x, sRs[k]);
                     }
+                    if constexpr (TC) {
+                        // the solved row, split into tf32 hi/lo, at its row of the operand panel
+                        const int prow = rb + tid - m0;
+                        for (int k = 0; k < 32; ++k) {
+                            float h = 0.f, l = 0.f;
+                            if (k < kb) tc::split_tf32(re(row[k]), h, l);
+                            const uint32_t off = tc::sw128_offset(prow, k);
+                            *reinterpret_cast<float *>(p_hi + off) = h;
+                            *reinterpret_cast<float *>(p_lo + off) = l;
+                        }
+                    }
                 }
                 __syncthreads();
                 for (int idx = tid; idx < nrow * kb; idx += THREADS) {
@@ -173,81 +236,79 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
             const int mt = n - m0;
             if (mt <= 0) continue;
             if constexpr (TC) {
-                unsigned char *tbase = reinterpret_cast<unsigned char *>(sW);
-                tbase += (1024 - (tc::smem_u32(tbase) & 1023)) & 1023;
-                unsigned char *a_hi = tbase, *a_lo = tbase + 16384, *b_hi = tbase + 32768, *b_lo = tbase + 49152;
+                // Every lower 128 x 128 tile (bi >= bk) of L21*L21^T, in a flat list. The
+                // operands are rows of the resident panel; tile t accumulates in tensor-memory
+                // buffer t&1, so the MMAs of tile t run while the epilogue of tile t-1 reads
+                // buffer (t-1)&1 and subtracts it from the trailing matrix.
+                tc::fence_proxy_async_smem();
+                tc::fence_before_sync();
+                __syncthreads();
+                tc::fence_after_sync();
                 const uint32_t tmem = s_tmem;
                 const int warp = tid >> 5, lane = tid & 31;
                 const int ntile = (mt + 127) / 128;
-                // operand tile: rows R0..R0+127 of L21 (k < kb), zero-padded, split into tf32 hi/lo
-                auto load_tile = [&](int R0, unsigned char *hi, unsigned char *lo) {
-                    for (int idx = tid; idx < 128 * 32; idx += THREADS) {
-                        const int row = upper ? idx >> 5 : idx & 127;
-                        const int k = upper ? idx & 31 : idx >> 7;
-                        float v = 0.f;
-                        if (R0 + row < n && k < kb) v = S.get(R0 + row, j0 + k);
-                        float h, l;
-                        tc::split_tf32(v, h, l);
-                        const uint32_t off = tc::sw128_offset(row, k);
-                        *reinterpret_cast<float *>(hi + off) = h;
-                        *reinterpret_cast<float *>(lo + off) = l;
+                const int T_all = ntile * (ntile + 1) / 2;
+                const uint32_t s_hi = tc::smem_u32(p_hi), s_lo = tc::smem_u32(p_lo);
+                int bi = 0, bk = 0;                  // tile t (issue side)
+                int ei = 0, ek = 0;                  // tile t-1 (epilogue side)
+                for (int t = 0; t <= T_all; ++t) {
+                    if (t < T_all && tid == 0) {
+                        constexpr uint32_t idesc = tc::idesc_tf32(128, 128);
+                        const uint32_t d = tmem + static_cast<uint32_t>((t & 1) * 128);
+                        const uint32_t a_hi = s_hi + bi * 16384, a_lo = s_lo + bi * 16384;
+                        const uint32_t b_hi = s_hi + bk * 16384, b_lo = s_lo + bk * 16384;
+                        for (int st = 0; st < 4; ++st)
+                            tc::mma_tf32(d, tc::sdesc_sw128(a_hi + 32 * st), tc::sdesc_sw128(b_hi + 32 * st), idesc, st > 0);
+                        for (int st = 0; st < 4; ++st)
+                            tc::mma_tf32(d, tc::sdesc_sw128(a_hi + 32 * st), tc::sdesc_sw128(b_lo + 32 * st), idesc, true);
+                        for (int st = 0; st < 4; ++st)
+                            tc::mma_tf32(d, tc::sdesc_sw128(a_lo + 32 * st), tc::sdesc_sw128(b_hi + 32 * st), idesc, true);
+                        tc::mma_commit(&s_mbar[t & 1]);
                     }
-                };
-                for (int bi = 0; bi < ntile; ++bi) {
-                    const int I0 = m0 + bi * 128;
-                    load_tile(I0, a_hi, a_lo);
-                    for (int bk = 0; bk <= bi; ++bk) {
-                        const int K0 = m0 + bk * 128;
-                        const bool diag_tile = bk == bi;
-                        if (!diag_tile) load_tile(K0, b_hi, b_lo);
-                        tc::fence_proxy_async_smem();
-                        tc::fence_before_sync();
-                        __syncthreads();
-                        tc::fence_after_sync();
-                        if (tid == 0) {
-                            constexpr uint32_t idesc = tc::idesc_tf32(128, 128);
-                            const uint32_t sa_hi = tc::smem_u32(a_hi), sa_lo = tc::smem_u32(a_lo);
-                            const uint32_t sb_hi = tc::smem_u32(diag_tile ? a_hi : b_hi);
-                            const uint32_t sb_lo = tc::smem_u32(diag_tile ? a_lo : b_lo);
-                            for (int st = 0; st < 4; ++st)
-                                tc::mma_tf32(tmem, tc::sdesc_sw128(sa_hi + 32 * st), tc::sdesc_sw128(sb_hi + 32 * st), idesc,
-                                             st > 0);
-                            for (int st = 0; st < 4; ++st)
-                                tc::mma_tf32(tmem, tc::sdesc_sw128(sa_hi + 32 * st), tc::sdesc_sw128(sb_lo + 32 * st), idesc,
-                                             true);
-                            for (int st = 0; st < 4; ++st)
-                                tc::mma_tf32(tmem, tc::sdesc_sw128(sa_lo + 32 * st), tc::sdesc_sw128(sb_hi + 32 * st), idesc,
-                                             true);
-                            tc::mma_commit(&s_mbar);
-                        }
-                        const bool done = tc::mbar_wait(&s_mbar, mma_phase & 1, 1u << 22);
-                        ++mma_phase;
+                    if (t >= 1) {
+                        const int u = t - 1, buf = u & 1;
+                        const bool done = tc::mbar_wait(&s_mbar[buf], (mma_phases >> buf) & 1u, 1u << 22);
+                        mma_phases ^= 1u << buf;
                         tc::fence_after_sync();
                         if (!done) {
-                            // the tensor core did not finish within the bounded wait: report an
-                            // internal error for this item instead of hanging
                             if (tid == 0) { args.info[mat] = -1; s_fail = 1; }
                         } else {
-                            // epilogue: TMEM lanes = tile rows (warp w reads lanes 32*(w%4)..), the
-                            // two warp halves take column halves; subtract into the lower triangle
                             const int row = 32 * (warp & 3) + lane;
-                            const int gi = I0 + row;
+                            const int gi = m0 + ei * 128 + row;
+                            const int K0 = m0 + ek * 128;
 #pragma unroll
                             for (int cc = 0; cc < 2; ++cc) {
                                 const int c0 = 64 * (warp >> 2) + 32 * cc;
                                 float v[32];
-                                tc::tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + c0, v);
+                                tc::tmem_ld32(tmem + static_cast<uint32_t>(buf * 128) +
+                                                  (static_cast<uint32_t>(32 * (warp & 3)) << 16) + c0,
+                                              v);
+                                if (gi < n) {
+                                    float old[32];
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) {
-                                    const int gk = K0 + c0 + i;
-                                    if (gi < n && gk < n && gi >= gk) S.set(gi, gk, S.get(gi, gk) - v[i]);
+                                    for (int i = 0; i < 32; ++i) {
+                                        const int gk = K0 + c0 + i;
+                                        old[i] = (gk < n && gi >= gk) ? re(S.get(gi, gk)) : 0.f;
+                                    }
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i) {
+                                        const int gk = K0 + c0 + i;
+                                        if (gk < n && gi >= gk) S.set(gi, gk, from_real<T>(old[i] - v[i]));
+                                    }
                                 }
                             }
                         }
                         tc::fence_before_sync();
-                        __syncthreads();
-                        tc::fence_after_sync();
+                        ei = bi;
+                        ek = bk;
+                    } else {
+                        ei = bi;
+                        ek = bk;
                     }
+                    // advance the issue-side tile
+                    if (++bk > bi) { ++bi; bk = 0; }
+                    __syncthreads();
+                    tc::fence_after_sync();
                 }
                 if (s_fail) break;
                 continue;
@@ -308,7 +369,7 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
     if constexpr (TC) {
         tc::fence_before_sync();
         __syncthreads();
-        if ((tid >> 5) == 0) tc::tmem_dealloc(s_tmem, 128);
+        if ((tid >> 5) == 0) tc::tmem_dealloc(s_tmem, 256);
     }
 
     // ---------------------------------------------- solves (posv after success, potrs)

@@ -145,7 +145,7 @@ int rhs_per_pass(const KernelEntry &e, int op, int64_t nrhs) {
 bool can_run(const KernelEntry &e, int op, int64_t n, int64_t nrhs, const DeviceFacts &dev) {
     if (e.smem > dev.smem_optin) return false;
     if (op != OP_POTRF && e.rhs_max < 0) return false;  // factor-only variant
-    if (e.family == 1) return true;
+    if (e.family == 1) return e.cap == 0 || n <= e.cap;   // blocked: any n, or up to its panel capacity
     if (e.family == 2) return n <= e.cap;  // right-hand sides sit in their own registers
     return n + rhs_per_pass(e, op, nrhs) <= e.cap;
 }

@@ -97,7 +97,9 @@ constexpr KernelEntry tile_entry() {
 template <typename T, int NB, bool TC = false>
 constexpr KernelEntry blocked_entry() {
     using C = BlkCfg<T, NB, TC>;
-    return KernelEntry{1, 0, TC ? 1 : 0, NB, 0, 0, C::THREADS, 1, C::smem_bytes, &launch_blocked<T, NB, TC>};
+    // the tensor-core variant keeps the whole L21 panel in shared memory: n <= TC_MAXM + NB
+    return KernelEntry{1, 0, TC ? 1 : 0, NB, TC ? C::TC_MAXM + NB : 0, 0, C::THREADS, 1, C::smem_bytes,
+                       &launch_blocked<T, NB, TC>};
 }
 
 }  // namespace bl
