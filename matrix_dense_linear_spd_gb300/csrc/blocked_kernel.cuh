@@ -59,7 +59,10 @@ struct BlkCfg {
     // (TC_MAXM rows x 128 bytes each, 128-byte-swizzled K-major), next to the panel staging area
     static constexpr int TC_MAXM = 512;                        // trailing rows: n <= TC_MAXM + NB
     static constexpr size_t tc_panel = static_cast<size_t>(TC_MAXM) * 128;
-    static constexpr size_t tc_bytes = TC ? panel_bytes + 1024 + 2 * tc_panel : 0;
+    // epilogue staging: half a product tile (128 x 64 f32) with a padded row stride for Upper
+    static constexpr int TC_STG_LD = 68;
+    static constexpr size_t tc_stage = static_cast<size_t>(128) * TC_STG_LD * 4;
+    static constexpr size_t tc_bytes = TC ? panel_bytes + 1024 + 2 * tc_panel + tc_stage : 0;
     static constexpr size_t simt_work = panel_bytes > trail_bytes ? panel_bytes : trail_bytes;
     static constexpr size_t work_bytes = simt_work > tc_bytes ? simt_work : tc_bytes;
     static constexpr size_t off_diag = 0;
@@ -251,6 +254,10 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
                 const uint32_t s_hi = tc::smem_u32(p_hi), s_lo = tc::smem_u32(p_lo);
                 int bi = 0, bk = 0;                  // tile t (issue side)
                 int ei = 0, ek = 0;                  // tile t-1 (epilogue side)
+                float *stg = reinterpret_cast<float *>(p_lo + C::tc_panel);
+                // bulk adds need 16-byte aligned runs: lda a multiple of 4 and an aligned base
+                const bool bulk_ok = (S.lda % 4 == 0) && ((reinterpret_cast<uintptr_t>(S.A) & 15) == 0);
+                bool bulk_issued = false;
                 for (int t = 0; t <= T_all; ++t) {
                     if (t < T_all && tid == 0) {
                         constexpr uint32_t idesc = tc::idesc_tf32(128, 128);
@@ -273,29 +280,65 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
                         if (!done) {
                             if (tid == 0) { args.info[mat] = -1; s_fail = 1; }
                         } else {
+                            // Epilogue, half a tile (64 columns) at a time: TMEM -> registers ->
+                            // staging (negated) -> asynchronous bulk adds into the trailing matrix,
+                            // one contiguous run per column (Lower) or per row of S (Upper). Runs
+                            // that do not start on a 16-byte boundary are done element-wise.
                             const int row = 32 * (warp & 3) + lane;
-                            const int gi = m0 + ei * 128 + row;
-                            const int K0 = m0 + ek * 128;
-#pragma unroll
-                            for (int cc = 0; cc < 2; ++cc) {
-                                const int c0 = 64 * (warp >> 2) + 32 * cc;
+                            const int I0 = m0 + ei * 128, K0 = m0 + ek * 128;
+                            for (int h = 0; h < 2; ++h) {
+                                if (bulk_issued) { tc::bulk_wait_read_all(); bulk_issued = false; }
+                                __syncthreads();
+                                const int cl0 = 32 * (warp >> 2);            // column inside the half
                                 float v[32];
                                 tc::tmem_ld32(tmem + static_cast<uint32_t>(buf * 128) +
-                                                  (static_cast<uint32_t>(32 * (warp & 3)) << 16) + c0,
+                                                  (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 64 * h + cl0,
                                               v);
-                                if (gi < n) {
-                                    float old[32];
 #pragma unroll
-                                    for (int i = 0; i < 32; ++i) {
-                                        const int gk = K0 + c0 + i;
-                                        old[i] = (gk < n && gi >= gk) ? re(S.get(gi, gk)) : 0.f;
+                                for (int i = 0; i < 32; ++i) {
+                                    if (!upper) stg[(cl0 + i) * 128 + row] = -v[i];
+                                    else stg[row * C::TC_STG_LD + cl0 + i] = -v[i];
+                                }
+                                tc::fence_proxy_async_smem();
+                                __syncthreads();
+                                if (!upper) {
+                                    if (tid < 64) {
+                                        const int gk = K0 + 64 * h + tid;
+                                        const int lo = max(I0, gk), hi = min(I0 + 128, n);
+                                        if (gk < n && lo < hi) {
+                                            float *colp = S.A + static_cast<int64_t>(gk) * S.lda;
+                                            const float *src = stg + tid * 128 - I0;
+                                            int la = lo, ha = lo;
+                                            if (bulk_ok) {
+                                                la = min((lo + 3) & ~3, hi);
+                                                ha = max(la, hi & ~3);
+                                            }
+                                            for (int gi = lo; gi < la; ++gi) colp[gi] += src[gi];
+                                            if (ha > la) {
+                                                tc::bulk_reduce_add_f32(colp + la, src + la, static_cast<uint32_t>((ha - la) * 4));
+                                                bulk_issued = true;
+                                            }
+                                            for (int gi = max(ha, la); gi < hi; ++gi) colp[gi] += src[gi];
+                                        }
                                     }
-#pragma unroll
-                                    for (int i = 0; i < 32; ++i) {
-                                        const int gk = K0 + c0 + i;
-                                        if (gk < n && gi >= gk) S.set(gi, gk, from_real<T>(old[i] - v[i]));
+                                } else {
+                                    if (tid < 128) {
+                                        const int gi = I0 + tid;
+                                        const int lo = K0 + 64 * h, hi = min(min(lo + 64, gi + 1), n);
+                                        if (gi < n && lo < hi) {
+                                            float *rowp = S.A + static_cast<int64_t>(gi) * S.lda;
+                                            const float *src = stg + tid * C::TC_STG_LD - lo;
+                                            int ha = lo;
+                                            if (bulk_ok) ha = lo + ((hi - lo) & ~3);
+                                            if (ha > lo) {
+                                                tc::bulk_reduce_add_f32(rowp + lo, src + lo, static_cast<uint32_t>((ha - lo) * 4));
+                                                bulk_issued = true;
+                                            }
+                                            for (int gk = ha; gk < hi; ++gk) rowp[gk] += src[gk];
+                                        }
                                     }
                                 }
+                                if (bulk_issued) tc::bulk_commit();
                             }
                         }
                         tc::fence_before_sync();
@@ -310,6 +353,10 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
                     __syncthreads();
                     tc::fence_after_sync();
                 }
+                // the bulk adds must have landed before anyone reads the trailing matrix again
+                if (bulk_issued) tc::bulk_wait_all();
+                tc::fence_proxy_async_all();
+                __syncthreads();
                 if (s_fail) break;
                 continue;
             }

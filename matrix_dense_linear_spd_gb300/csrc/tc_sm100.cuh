@@ -127,6 +127,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// ---- bulk (TMA) reduction: global[0..bytes) += shared[0..bytes), f32, performed by L2.
+// Both addresses 16-byte aligned, bytes a multiple of 16. Completion is tracked per thread by
+// bulk groups: commit after issuing, wait_group.read 0 before the source may be rewritten,
+// wait_group 0 before other threads may read the destination (then fence.proxy.async).
+__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const float *ssrc, uint32_t bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;\n" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;\n" ::: "memory"); }
+
 // Split an f32 value into tf32 hi and lo parts (x ~= hi + lo to about 2^-22 relative): hi is x
 // rounded to tf32, lo the rounded remainder (both kept as f32 bit patterns; the tensor core
 // reads the top 19 bits).
