@@ -257,7 +257,8 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
                 float *stg = reinterpret_cast<float *>(p_lo + C::tc_panel);
                 // bulk adds need 16-byte aligned runs: lda a multiple of 4 and an aligned base
                 const bool bulk_ok = (S.lda % 4 == 0) && ((reinterpret_cast<uintptr_t>(S.A) & 15) == 0);
-                bool bulk_issued = false;
+                bool bulk_issued = false;            // issued since the last read-completion wait
+                bool bulk_pending = false;           // issued since the last full-completion wait
                 for (int t = 0; t <= T_all; ++t) {
                     if (t < T_all && tid == 0) {
                         constexpr uint32_t idesc = tc::idesc_tf32(128, 128);
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
                                             for (int gi = lo; gi < la; ++gi) colp[gi] += src[gi];
                                             if (ha > la) {
                                                 tc::bulk_reduce_add_f32(colp + la, src + la, static_cast<uint32_t>((ha - la) * 4));
-                                                bulk_issued = true;
+                                                bulk_issued = bulk_pending = true;
                                             }
                                             for (int gi = max(ha, la); gi < hi; ++gi) colp[gi] += src[gi];
                                         }
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
                                             if (bulk_ok) ha = lo + ((hi - lo) & ~3);
                                             if (ha > lo) {
                                                 tc::bulk_reduce_add_f32(rowp + lo, src + lo, static_cast<uint32_t>((ha - lo) * 4));
-                                                bulk_issued = true;
+                                                bulk_issued = bulk_pending = true;
                                             }
                                             for (int gk = ha; gk < hi; ++gk) rowp[gk] += src[gk];
                                         }
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
                     tc::fence_after_sync();
                 }
                 // the bulk adds must have landed before anyone reads the trailing matrix again
-                if (bulk_issued) tc::bulk_wait_all();
+                if (bulk_pending) tc::bulk_wait_all();
                 tc::fence_proxy_async_all();
                 __syncthreads();
                 if (s_fail) break;
