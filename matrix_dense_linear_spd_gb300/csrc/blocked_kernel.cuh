@@ -72,7 +72,7 @@ struct BlkCfg {
 };
 
 template <typename T, int NB, bool TC = false>
-__global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
+__global__ void __launch_bounds__(256, TC ? 1 : 2) blocked_kernel(const BatchArgs args) {
     using C = BlkCfg<T, NB, TC>;
     using R = typename C::R;
     constexpr int THREADS = C::THREADS, TB = C::TB, LDD = C::LDD, LDP = C::LDP, LDT = C::LDT;
@@ -145,9 +145,12 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
                         }
                         if (lane == j) sRs[j] = rs;
                     }
+                    float *sL = reinterpret_cast<float *>(sW);        // L11 columns, stride 32
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
+                    for (int c = 0; c < 32; ++c) {
                         if (c <= lane && lane < kb) sD[c * LDD + lane] = a[c];
+                        sL[c * 32 + lane] = (c < lane && lane < kb) ? a[c] : 0.f;
+                    }
                     if (lane == 0) s_diag_fail = failed ? __ffs(failed) - 1 : -1;
                 }
                 __syncthreads();
@@ -198,6 +201,48 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
                     *reinterpret_cast<float *>(p_lo + off) = 0.f;
                 }
             }
+            if constexpr (TC) {
+                // one row of A21 per thread, in registers: x_k = a_k / L(k,k), then
+                // a_m -= x_k * L(m,k) for m > k (independent FMAs), L11 columns read as 16-byte
+                // broadcasts; the solved row goes back to memory and, split into tf32 hi/lo, into
+                // its row of the resident operand panels as 16-byte chunks
+                const float *sL = reinterpret_cast<const float *>(sW);
+                for (int rb = m0; rb < n; rb += THREADS) {
+                    const int r = rb + tid;
+                    if (r < n) {
+                        float a[32];
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) a[k] = re(S.get(r, j0 + k));
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const float x = a[k] * sRs[k];
+                            a[k] = x;
+#pragma unroll
+                            for (int q = (k + 1) / 4; q < 8; ++q) {
+                                const float4 l4 = *reinterpret_cast<const float4 *>(sL + k * 32 + 4 * q);
+                                if (4 * q + 0 > k) a[4 * q + 0] = fmaf(-x, l4.x, a[4 * q + 0]);
+                                if (4 * q + 1 > k) a[4 * q + 1] = fmaf(-x, l4.y, a[4 * q + 1]);
+                                if (4 * q + 2 > k) a[4 * q + 2] = fmaf(-x, l4.z, a[4 * q + 2]);
+                                if (4 * q + 3 > k) a[4 * q + 3] = fmaf(-x, l4.w, a[4 * q + 3]);
+                            }
+                        }
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) S.set(r, j0 + k, from_real<T>(a[k]));
+                        const int prow = r - m0;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            float4 h4, l4;
+                            tc::split_tf32(a[4 * q + 0], h4.x, l4.x);
+                            tc::split_tf32(a[4 * q + 1], h4.y, l4.y);
+                            tc::split_tf32(a[4 * q + 2], h4.z, l4.z);
+                            tc::split_tf32(a[4 * q + 3], h4.w, l4.w);
+                            const uint32_t off = tc::sw128_offset(prow, 4 * q);
+                            *reinterpret_cast<float4 *>(p_hi + off) = h4;
+                            *reinterpret_cast<float4 *>(p_lo + off) = l4;
+                        }
+                    }
+                }
+            } else
             for (int rb = m0; rb < n; rb += THREADS) {
                 const int nrow = min(THREADS, n - rb);
                 for (int idx = tid; idx < nrow * kb; idx += THREADS) {
@@ -213,17 +258,6 @@ __global__ void __launch_bounds__(256) blocked_kernel(const BatchArgs args) {
                         T x = row[k];
                         for (int m = 0; m < k; ++m) sub_mul_conj(x, row[m], sD[m * LDD + k]);
                         row[k] = scale(x, sRs[k]);
-                    }
-                    if constexpr (TC) {
-                        // the solved row, split into tf32 hi/lo, at its row of the operand panel
-                        const int prow = rb + tid - m0;
-                        for (int k = 0; k < 32; ++k) {
-                            float h = 0.f, l = 0.f;
-                            if (k < kb) tc::split_tf32(re(row[k]), h, l);
-                            const uint32_t off = tc::sw128_offset(prow, k);
-                            *reinterpret_cast<float *>(p_hi + off) = h;
-                            *reinterpret_cast<float *>(p_lo + off) = l;
-                        }
                     }
                 }
                 __syncthreads();
