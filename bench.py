@@ -181,26 +181,26 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_source_sha():
+def kernel_source_sha(files):
+    """Short hash of the kernel source files a measured kernel is built from."""
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "matrix_dense_linear_spd_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cuh", ".cu", ".cpp", ".h")) and not f.startswith("_"):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in files:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel_tag: str):
-    """dram bytes per launch from the committed ncu summary, if it was taken on the current
-    kernel sources; else None."""
+    """DRAM bytes per launch (read + write) from the committed ncu record, if it was taken on
+    the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(kernel_tag)
-    if not e or e.get("source_sha") != kernel_source_sha():
+    if not e or e.get("source_sha") != kernel_source_sha(e.get("source_files", [])):
         return None
     return e.get("dram_bytes_per_launch")
 

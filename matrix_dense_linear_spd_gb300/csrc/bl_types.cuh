@@ -27,6 +27,11 @@ __device__ __forceinline__ double re(double v) { return v; }
 __device__ __forceinline__ float re(cf32 v) { return v.x; }
 __device__ __forceinline__ double re(cf64 v) { return v.x; }
 
+__device__ __forceinline__ float im_part(float) { return 0.f; }
+__device__ __forceinline__ double im_part(double) { return 0.0; }
+__device__ __forceinline__ float im_part(cf32 v) { return v.y; }
+__device__ __forceinline__ double im_part(cf64 v) { return v.y; }
+
 template <typename T> __device__ __forceinline__ T zero();
 template <> __device__ __forceinline__ float zero<float>() { return 0.f; }
 template <> __device__ __forceinline__ double zero<double>() { return 0.0; }

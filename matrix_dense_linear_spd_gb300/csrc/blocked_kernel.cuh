@@ -72,7 +72,7 @@ struct BlkCfg {
 };
 
 template <typename T, int NB, bool TC = false>
-__global__ void __launch_bounds__(256, TC ? 1 : 2) blocked_kernel(const BatchArgs args) {
+__global__ void __launch_bounds__(256, TC ? 1 : 4) blocked_kernel(const BatchArgs args) {
     using C = BlkCfg<T, NB, TC>;
     using R = typename C::R;
     constexpr int THREADS = C::THREADS, TB = C::TB, LDD = C::LDD, LDP = C::LDP, LDT = C::LDT;

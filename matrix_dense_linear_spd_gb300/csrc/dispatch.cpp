@@ -75,6 +75,7 @@ std::string spelling(const KernelEntry &e) {
     char buf[64];
     if (e.family == 0) snprintf(buf, sizeof buf, "tile:p=%d:s=%d", e.p, e.s);
     else if (e.family == 2) snprintf(buf, sizeof buf, "warp:p=%d:r=%d", e.p, e.s);
+    else if (e.family == 3) snprintf(buf, sizeof buf, "thread:n=%d", e.nb);
     else if (e.s) snprintf(buf, sizeof buf, "blocked:nb=%d:tc=1", e.nb);   // tensor-core trailing update
     else snprintf(buf, sizeof buf, "blocked:nb=%d", e.nb);
     return buf;
@@ -94,7 +95,7 @@ std::string canon(std::string s) {
     while (std::getline(ss, tok, ':')) parts.push_back(tok);
     if (parts.empty()) return s;
     static const std::map<std::string, std::vector<std::string>> fields = {
-        {"tile", {"p", "s"}}, {"warp", {"p", "r"}}, {"blocked", {"nb", "tc"}}};
+        {"tile", {"p", "s"}}, {"warp", {"p", "r"}}, {"blocked", {"nb", "tc"}}, {"thread", {"n"}}};
     auto it = fields.find(parts[0]);
     if (it == fields.end()) return s;
     std::string out = parts[0];
@@ -146,7 +147,7 @@ bool can_run(const KernelEntry &e, int op, int64_t n, int64_t nrhs, const Device
     if (e.smem > dev.smem_optin) return false;
     if (op != OP_POTRF && e.rhs_max < 0) return false;  // factor-only variant
     if (e.family == 1) return e.cap == 0 || n <= e.cap;   // blocked: any n, or up to its panel capacity
-    if (e.family == 2) return n <= e.cap;  // right-hand sides sit in their own registers
+    if (e.family == 2 || e.family == 3) return n <= e.cap;  // right-hand sides do not take rows
     return n + rhs_per_pass(e, op, nrhs) <= e.cap;
 }
 

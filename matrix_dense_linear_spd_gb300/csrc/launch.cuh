@@ -9,6 +9,7 @@
 #include "blocked_kernel.cuh"
 #include "tile_kernel.cuh"
 #include "warp_kernel.cuh"
+#include "thread_kernel.cuh"
 
 namespace bl {
 
@@ -86,6 +87,23 @@ template <typename T, int P, int R>
 constexpr KernelEntry warp_entry() {
     using C = WarpCfg<T, P, R>;
     return KernelEntry{2, P, R, 0, C::N, C::RHS, C::THREADS, C::PER_CTA, C::smem_solve, &launch_warp<T, P, R>};
+}
+
+template <typename T, int NMAX>
+cudaError_t launch_thread(const BatchArgs &a, cudaStream_t st) {
+    using C = ThreadCfg<T, NMAX>;
+    static std::atomic<unsigned long long> done{0};
+    cudaError_t e = ensure_smem(thread_kernel<T, NMAX>, C::smem_bytes, done);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>((a.batch + C::THREADS - 1) / C::THREADS);
+    thread_kernel<T, NMAX><<<grid, C::THREADS, C::smem_bytes, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int NMAX>
+constexpr KernelEntry thread_entry() {
+    using C = ThreadCfg<T, NMAX>;
+    return KernelEntry{3, 0, 0, NMAX, NMAX, -1, C::THREADS, C::THREADS, C::smem_bytes, &launch_thread<T, NMAX>};
 }
 
 template <typename T, int P, int S>
