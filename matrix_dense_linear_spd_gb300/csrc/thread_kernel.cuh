@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(128, 1) thread_kernel(const BatchArgs args) {
     const int n = args.n;
     const bool upper = args.upper != 0;
     const int64_t m0 = static_cast<int64_t>(blockIdx.x) * THREADS;
-    const int nm = static_cast<int>(min<int64_t>(THREADS, args.batch - m0));   // live matrices
+    const int nm = static_cast<int>(args.batch - m0 < THREADS ? args.batch - m0 : THREADS);   // live matrices
     const T *A = static_cast<const T *>(args.A);
     const int64_t lda = args.lda, sa = args.stride_a;
     const int nn = n * n;

@@ -95,7 +95,13 @@ def test_can_run_is_capacity_only(bl):
                     assert bl.select_debug("potrf", dt, "U", 1000, 0, 7).startswith(sp + " [pin]")
             finally:
                 bl.set_route("potrf", None)
-            if cap and sp.startswith("warp"):   # right-hand sides do not take tile rows
+            if cap and rhs < 0:                  # factor-only variant: a solve pin is refused
+                bl.set_route("posv", sp)
+                try:
+                    assert bl.select_debug("posv", dt, "L", 2, 1, 7).startswith("error:")
+                finally:
+                    bl.set_route("posv", None)
+            elif cap and sp.startswith("warp"):   # right-hand sides do not take tile rows
                 bl.set_route("posv", sp)
                 try:
                     assert bl.select_debug("posv", dt, "L", cap, 50, 7).startswith(sp)
