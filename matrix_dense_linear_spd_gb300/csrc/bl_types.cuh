@@ -95,6 +95,22 @@ __device__ __forceinline__ void add_into(cf64 &a, cf64 b) { a.x += b.x; a.y += b
 __device__ __forceinline__ float rsqrt_of(float d) { return rsqrtf(d); }
 __device__ __forceinline__ double rsqrt_of(double d) { return rsqrt(d); }
 
+// Asynchronous global -> shared copies (cp.async): no register round trip; completion by
+// commit groups.
+__device__ __forceinline__ unsigned smem_addr(const void *p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+template <int BYTES>
+__device__ __forceinline__ void cp_async_elem(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;\n" ::"r"(smem_addr(dst)), "l"(src), "n"(BYTES)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
 // Operation selector shared by the kernels.
 enum Mode : int { MODE_POTRF = 0, MODE_POSV = 1, MODE_POTRS = 2 };
 

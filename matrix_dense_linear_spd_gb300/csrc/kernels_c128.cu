@@ -8,6 +8,7 @@ namespace bl {
 static const KernelEntry k_entries_c128[] = {
     thread_entry<cf64, 8>(),
     thread_entry<cf64, 12>(),
+    thread_entry<cf64, 18>(),
     warp_entry<cf64, 4, 2>(),
     warp_entry<cf64, 8, 1>(),
     warp_entry<cf64, 8, 2>(),

@@ -5,15 +5,20 @@
 // non-positive pivot, Upper as a load/store transform): Cholesky-Banachiewicz, row by row --
 //   L(i,j) = (A(i,j) - sum_{k<j} L(i,k) * conj(L(j,k))) / L(j,j),  j < i,
 //   d = Re A(i,i) - sum_{k<i} |L(i,k)|^2;  stop with info = i+1 if !(d > 0), else L(i,i) = sqrt(d).
+// Upper runs the same recurrence on S(i,j) = conj(A(j,i)); the conjugation is applied where each
+// input value is first read, so the copy into shared memory is a plain byte copy.
 //
 // Why a thread per matrix: GB300 executes FP64 at 2 lanes per clock per SM, 1/64 of its FP32
 // rate, so every f64 cell is bound by FP64 instructions issued, and any layout that spreads
 // one small matrix over many lanes (predicated-off or padded lanes still occupy the FP64 pipe)
-// wastes most of it. Here every lane of every FP64 instruction does useful work. One warp per
-// SM sub-partition keeps the FP64 units busy: a warp-wide FP64 instruction occupies its unit
-// for 16 clocks, far longer than any dependency latency. Loads and stores are cooperative and
-// coalesced (the CTA's matrices are one contiguous range in the common layout); the packed
-// stride is odd in 8-byte words so per-thread accesses are bank-conflict free.
+// wastes most of it. Here every lane of every FP64 instruction does useful work, and a few warps
+// per SM keep the FP64 pipe busy (a warp-wide FP64 instruction holds it for 16 clocks).
+//
+// Data movement: the CTA's triangles arrive by asynchronous element copies (cp.async, no
+// register round trip, all in flight at once) in global-address order, so a warp's copies are
+// coalesced; a per-CTA table maps each position of an n x n item to its packed slot, so the
+// copy loop needs no division. The packed stride is odd in 8-byte words, so the per-thread
+// accesses of the factorisation are bank-conflict free.
 #pragma once
 
 #include "bl_types.cuh"
@@ -22,47 +27,66 @@ namespace bl {
 
 template <typename T, int NMAX>
 struct ThreadCfg {
-    static constexpr int THREADS = 128;
     static constexpr int TRI = NMAX * (NMAX + 1) / 2;            // packed lower triangle, row-major
-    static constexpr int WORDS = static_cast<int>(sizeof(T) / 4);
     // packed triangle + NMAX reciprocal pivots; stride odd in 8-byte units (conflict-free)
     static constexpr int rsw = (NMAX * static_cast<int>(sizeof(real_t<T>)) + static_cast<int>(sizeof(T)) - 1) /
                                static_cast<int>(sizeof(T));
     static constexpr int PACK0 = TRI + rsw;
     static constexpr int PACK = (((PACK0 * static_cast<int>(sizeof(T))) / 8) % 2) ? PACK0 : PACK0 + 1;
-    static constexpr size_t smem_bytes = sizeof(T) * static_cast<size_t>(PACK) * THREADS;
+    static constexpr size_t table_bytes = sizeof(uint32_t) * NMAX * NMAX;
+    static constexpr size_t bytes_for(int threads) { return sizeof(T) * static_cast<size_t>(PACK) * threads + table_bytes; }
+    // as many matrices per CTA as fit one CTA's shared memory, up to 128
+    static constexpr int THREADS = bytes_for(128) <= 227 * 1024 ? 128 : 64;
+    static constexpr size_t smem_bytes = bytes_for(THREADS);
 };
 
 __device__ __forceinline__ int tri_idx(int i, int j) { return i * (i + 1) / 2 + j; }
 
 template <typename T, int NMAX>
-__global__ void __launch_bounds__(128, 1) thread_kernel(const BatchArgs args) {
+__global__ void __launch_bounds__(ThreadCfg<T, NMAX>::THREADS, 1) thread_kernel(const BatchArgs args) {
     using C = ThreadCfg<T, NMAX>;
     using R = real_t<T>;
     constexpr int THREADS = C::THREADS, PACK = C::PACK, TRI = C::TRI;
     extern __shared__ __align__(16) unsigned char smem[];
     T *sm = reinterpret_cast<T *>(smem);
+    uint32_t *tab = reinterpret_cast<uint32_t *>(smem + sizeof(T) * static_cast<size_t>(PACK) * THREADS);
 
     const int tid = threadIdx.x;
     const int n = args.n;
     const bool upper = args.upper != 0;
     const int64_t m0 = static_cast<int64_t>(blockIdx.x) * THREADS;
     const int nm = static_cast<int>(args.batch - m0 < THREADS ? args.batch - m0 : THREADS);   // live matrices
-    const T *A = static_cast<const T *>(args.A);
     const int64_t lda = args.lda, sa = args.stride_a;
     const int nn = n * n;
 
-    // ---- cooperative load of the referenced triangles (contiguous index fastest)
-    for (int idx = tid; idx < nm * nn; idx += THREADS) {
-        const int mm = idx / nn, rem = idx - mm * nn;
-        const int col = rem / n, row = rem - col * n;                 // A(row, col)
-        const T v = A[(m0 + mm) * sa + static_cast<int64_t>(col) * lda + row];
-        if (!upper) {
-            if (row >= col) sm[mm * PACK + tri_idx(row, col)] = v;
-        } else {
-            if (row <= col) sm[mm * PACK + tri_idx(col, row)] = conj(v);   // S(col,row) = conj(A(row,col))
+    // position rem = col * n + row of the n x n item -> bits 0-15 its packed slot (0xFFFF: not
+    // referenced), bits 16-23 col, bits 24-31 row
+    for (int rem = tid; rem < nn; rem += THREADS) {
+        const int col = rem / n, row = rem - col * n;
+        const bool ref = upper ? row <= col : row >= col;
+        const uint32_t slot = ref ? static_cast<uint32_t>(upper ? tri_idx(col, row) : tri_idx(row, col)) : 0xFFFFu;
+        tab[rem] = slot | (static_cast<uint32_t>(col) << 16) | (static_cast<uint32_t>(row) << 24);
+    }
+    __syncthreads();
+
+    // flat index idx = mm * nn + rem over the CTA's items, walked in steps of THREADS without division
+    const int dm = THREADS / nn, dr = THREADS - (THREADS / nn) * nn;
+    const T *A = static_cast<const T *>(args.A) + m0 * sa;
+    {
+        int mm = tid / nn, rem = tid - (tid / nn) * nn;
+        for (int idx = tid; idx < nm * nn; idx += THREADS) {
+            const uint32_t e = tab[rem];
+            const uint32_t slot = e & 0xFFFFu;
+            if (slot != 0xFFFFu) {
+                const int col = (e >> 16) & 0xFF, row = e >> 24;
+                cp_async_elem<sizeof(T)>(sm + mm * PACK + slot, A + mm * sa + col * lda + row);
+            }
+            mm += dm;
+            rem += dr;
+            if (rem >= nn) rem -= nn, ++mm;
         }
     }
+    cp_async_wait_all();
     __syncthreads();
 
     // ---- one matrix per thread
@@ -74,15 +98,28 @@ __global__ void __launch_bounds__(128, 1) thread_kernel(const BatchArgs args) {
             T *ri = a + tri_idx(i, 0);
             for (int j = 0; j < i; ++j) {
                 const T *rj = a + tri_idx(j, 0);
-                T s = ri[j];
-                for (int k = 0; k < j; ++k) sub_mul_conj(s, ri[k], rj[k]);
-                ri[j] = scale(s, rinv[j]);
+                T s0 = upper ? conj(ri[j]) : ri[j], s1 = zero<T>();
+                int k = 0;
+                for (; k + 1 < j; k += 2) {               // two partial sums halve the dependency chain
+                    sub_mul_conj(s0, ri[k], rj[k]);
+                    sub_mul_conj(s1, ri[k + 1], rj[k + 1]);
+                }
+                if (k < j) sub_mul_conj(s0, ri[k], rj[k]);
+                add_into(s0, s1);
+                ri[j] = scale(s0, rinv[j]);
             }
-            R d = re(ri[i]);
-            for (int k = 0; k < i; ++k) {
+            R d0 = re(ri[i]), d1 = R(0);
+            int k = 0;
+            for (; k + 1 < i; k += 2) {
+                const T v = ri[k], w = ri[k + 1];
+                d0 -= re(v) * re(v) + (is_cplx<T>::value ? im_part(v) * im_part(v) : R(0));
+                d1 -= re(w) * re(w) + (is_cplx<T>::value ? im_part(w) * im_part(w) : R(0));
+            }
+            if (k < i) {
                 const T v = ri[k];
-                d -= re(v) * re(v) + (is_cplx<T>::value ? im_part(v) * im_part(v) : R(0));
+                d0 -= re(v) * re(v) + (is_cplx<T>::value ? im_part(v) * im_part(v) : R(0));
             }
+            const R d = d0 + d1;
             if (!(d > R(0))) {
                 info = i + 1;
                 break;
@@ -94,15 +131,21 @@ __global__ void __launch_bounds__(128, 1) thread_kernel(const BatchArgs args) {
     }
     __syncthreads();
 
-    // ---- cooperative store of the referenced triangles
-    T *Aw = static_cast<T *>(args.A);
-    for (int idx = tid; idx < nm * nn; idx += THREADS) {
-        const int mm = idx / nn, rem = idx - mm * nn;
-        const int col = rem / n, row = rem - col * n;
-        if (!upper) {
-            if (row >= col) Aw[(m0 + mm) * sa + static_cast<int64_t>(col) * lda + row] = sm[mm * PACK + tri_idx(row, col)];
-        } else {
-            if (row <= col) Aw[(m0 + mm) * sa + static_cast<int64_t>(col) * lda + row] = conj(sm[mm * PACK + tri_idx(col, row)]);
+    // ---- store of the referenced triangles, same walk (coalesced global writes)
+    T *Aw = static_cast<T *>(args.A) + m0 * sa;
+    {
+        int mm = tid / nn, rem = tid - (tid / nn) * nn;
+        for (int idx = tid; idx < nm * nn; idx += THREADS) {
+            const uint32_t e = tab[rem];
+            const uint32_t slot = e & 0xFFFFu;
+            if (slot != 0xFFFFu) {
+                const int col = (e >> 16) & 0xFF, row = e >> 24;
+                const T v = sm[mm * PACK + slot];
+                Aw[mm * sa + col * lda + row] = upper ? conj(v) : v;
+            }
+            mm += dm;
+            rem += dr;
+            if (rem >= nn) rem -= nn, ++mm;
         }
     }
     if (tid < nm) args.info[m0 + tid] = info;

@@ -33,20 +33,6 @@
 
 namespace bl {
 
-__device__ __forceinline__ unsigned smem_addr(const void *p) {
-    return static_cast<unsigned>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
-template <int BYTES>
-__device__ __forceinline__ void cp_async_elem(void *dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;\n" ::"r"(smem_addr(dst)), "l"(src), "n"(BYTES)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
-
 // Compacted per-matrix slab for an N x N item, in chunks of E elements (16 bytes).
 //   Lower: column c keeps rows [E*floor(c/E), N)        (the chunks meeting rows >= c)
 //   Upper: column c keeps rows [0, E*ceil((c+1)/E))     (the chunks meeting rows <= c)
