@@ -70,6 +70,12 @@ __device__ __forceinline__ void sub_mul_conj(cf64 &acc, cf64 a, cf64 b) {
     acc.y = fma(a.x, b.y, acc.y);
 }
 
+// acc -= |a|^2 (acc real)
+__device__ __forceinline__ void sub_abs2(float &acc, float a) { acc = fmaf(-a, a, acc); }
+__device__ __forceinline__ void sub_abs2(double &acc, double a) { acc = fma(-a, a, acc); }
+__device__ __forceinline__ void sub_abs2(float &acc, cf32 a) { acc = fmaf(-a.y, a.y, fmaf(-a.x, a.x, acc)); }
+__device__ __forceinline__ void sub_abs2(double &acc, cf64 a) { acc = fma(-a.y, a.y, fma(-a.x, a.x, acc)); }
+
 // acc -= a * b
 __device__ __forceinline__ void sub_mul(float &acc, float a, float b) { acc = fmaf(-a, b, acc); }
 __device__ __forceinline__ void sub_mul(double &acc, double a, double b) { acc = fma(-a, b, acc); }

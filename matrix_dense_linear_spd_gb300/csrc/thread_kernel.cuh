@@ -89,18 +89,46 @@ __global__ void __launch_bounds__(ThreadCfg<T, NMAX>::THREADS, 1) thread_kernel(
     cp_async_wait_all();
     __syncthreads();
 
-    // ---- one matrix per thread
+    // ---- one matrix per thread. Two entries of row i at a time (j, j+1): the shared loads of
+    // L(i,k) feed both dot products, and each is split in two partial sums, so four independent
+    // FP64 chains are in flight per thread (the FP64 pipe's latency is long).
     int info = 0;
     if (tid < nm) {
         T *a = sm + tid * PACK;
         R *rinv = reinterpret_cast<R *>(a + TRI);
         for (int i = 0; i < n; ++i) {
             T *ri = a + tri_idx(i, 0);
-            for (int j = 0; j < i; ++j) {
+            int j = 0;
+            for (; j + 1 < i; j += 2) {
+                const T *rj = a + tri_idx(j, 0);
+                const T *rj1 = rj + j + 1;                    // row j+1 follows row j
+                T sa0 = upper ? conj(ri[j]) : ri[j], sb0 = upper ? conj(ri[j + 1]) : ri[j + 1];
+                T sa1 = zero<T>(), sb1 = zero<T>();
+                int k = 0;
+                for (; k + 1 < j; k += 2) {
+                    const T x0 = ri[k], x1 = ri[k + 1];
+                    sub_mul_conj(sa0, x0, rj[k]);
+                    sub_mul_conj(sb0, x0, rj1[k]);
+                    sub_mul_conj(sa1, x1, rj[k + 1]);
+                    sub_mul_conj(sb1, x1, rj1[k + 1]);
+                }
+                if (k < j) {
+                    const T x0 = ri[k];
+                    sub_mul_conj(sa0, x0, rj[k]);
+                    sub_mul_conj(sb0, x0, rj1[k]);
+                }
+                add_into(sa0, sa1);
+                add_into(sb0, sb1);
+                const T lij = scale(sa0, rinv[j]);
+                ri[j] = lij;
+                sub_mul_conj(sb0, lij, rj1[j]);
+                ri[j + 1] = scale(sb0, rinv[j + 1]);
+            }
+            if (j < i) {                                      // odd leftover entry j = i-1
                 const T *rj = a + tri_idx(j, 0);
                 T s0 = upper ? conj(ri[j]) : ri[j], s1 = zero<T>();
                 int k = 0;
-                for (; k + 1 < j; k += 2) {               // two partial sums halve the dependency chain
+                for (; k + 1 < j; k += 2) {
                     sub_mul_conj(s0, ri[k], rj[k]);
                     sub_mul_conj(s1, ri[k + 1], rj[k + 1]);
                 }
@@ -108,24 +136,22 @@ __global__ void __launch_bounds__(ThreadCfg<T, NMAX>::THREADS, 1) thread_kernel(
                 add_into(s0, s1);
                 ri[j] = scale(s0, rinv[j]);
             }
-            R d0 = re(ri[i]), d1 = R(0);
+            R d0 = re(ri[i]), d1 = R(0), d2 = R(0), d3 = R(0);
             int k = 0;
-            for (; k + 1 < i; k += 2) {
-                const T v = ri[k], w = ri[k + 1];
-                d0 -= re(v) * re(v) + (is_cplx<T>::value ? im_part(v) * im_part(v) : R(0));
-                d1 -= re(w) * re(w) + (is_cplx<T>::value ? im_part(w) * im_part(w) : R(0));
+            for (; k + 3 < i; k += 4) {
+                sub_abs2(d0, ri[k]);
+                sub_abs2(d1, ri[k + 1]);
+                sub_abs2(d2, ri[k + 2]);
+                sub_abs2(d3, ri[k + 3]);
             }
-            if (k < i) {
-                const T v = ri[k];
-                d0 -= re(v) * re(v) + (is_cplx<T>::value ? im_part(v) * im_part(v) : R(0));
-            }
-            const R d = d0 + d1;
-            if (!(d > R(0))) {
+            for (; k < i; ++k) sub_abs2(d0, ri[k]);
+            const R dd = (d0 + d1) + (d2 + d3);
+            if (!(dd > R(0))) {
                 info = i + 1;
                 break;
             }
-            const R r = rsqrt_of(d);
-            ri[i] = from_real<T>(d * r);
+            const R r = rsqrt_of(dd);
+            ri[i] = from_real<T>(dd * r);
             rinv[i] = r;
         }
     }
