@@ -136,8 +136,9 @@ __device__ __forceinline__ int lower_slab_offset(int c) {
 }
 
 // Issue the asynchronous copy of group `grp`'s referenced triangles into the warp's slab.
-// Lanes map to fixed (matrix, 16-byte chunk) pairs and sweep the columns at run time, so the
-// copy costs a handful of registers, not one address per chunk.
+// Lanes map to fixed (matrix, chunk) or (matrix, row) pairs and sweep the columns, so the copy
+// costs a handful of registers, not one address per chunk; 16-byte chunks when the layout
+// allows them, element copies otherwise.
 template <typename T, int P, int R>
 __device__ __forceinline__ void warp_prefetch(const BatchArgs &args, T *tri, int64_t grp, int lane, bool vec) {
     using C = WarpCfg<T, P, R>;
@@ -148,28 +149,44 @@ __device__ __forceinline__ void warp_prefetch(const BatchArgs &args, T *tri, int
     const T *A0 = static_cast<const T *>(args.A) + grp * G * sa;
     const int64_t mleft = args.batch - grp * G;            // live matrices in this group
     if (vec) {
+        // lanes map to fixed (matrix, 16-byte chunk) pairs; the column loop is unrolled so every
+        // slab offset is a compile-time constant, the source is one running pointer per sweep,
+        // and a lane's chunk takes part in the columns below one threshold (Lower: c < Q*E + E,
+        // the chunk meets rows >= c) or from one threshold on (Upper: c >= Q*E)
         constexpr int NQ = N / E;                          // chunks per full column
         constexpr int CPC = G * NQ;                        // (matrix, chunk) pairs per column
-        constexpr int CPI = CPC >= 32 ? 1 : 32 / CPC;      // columns per sweep step
-        constexpr int ITER = (CPI * CPC + 31) / 32;
-        for (int c0 = 0; c0 < n; c0 += CPI) {
+        constexpr int ITC = (CPC + 31) / 32;               // lane sweeps per column
+        const T *src[ITC];
+        int dst[ITC], lim[ITC];
 #pragma unroll
-            for (int it = 0; it < ITER; ++it) {
-                const int t = lane + 32 * it;
-                const int cc = t / CPC, rem = t - cc * CPC;
-                const int gg = rem / NQ, Q = rem - gg * NQ;
-                const int c = c0 + cc;
-                if (t >= CPI * CPC || c >= n || gg >= mleft) continue;
-                int pos;
-                if (!upper) {
-                    const int f = (c / E) * E;             // first kept row of column c
-                    if (Q * E < f || Q * E >= n) continue;
-                    pos = lower_slab_offset<N, E>(c) + Q * E - f;
-                } else {
-                    if (Q * E > c) continue;               // chunks meeting rows 0..c
-                    pos = upper_slab_offset(c, E) + Q * E;
+        for (int it = 0; it < ITC; ++it) {
+            const int t = lane + 32 * it;
+            const int gg = t / NQ, Q = t - gg * NQ;
+            const bool ok = t < CPC && gg < mleft && Q * E < n;
+            lim[it] = upper ? (ok ? Q * E : N) : (ok ? Q * E + E : 0);
+            src[it] = A0 + gg * sa + Q * E;
+            dst[it] = gg * MS + Q * E;
+        }
+        using L = TriSlab<N, E>;
+        if (!upper) {
+#pragma unroll
+            for (int c = 0; c < N; ++c) {
+                if (c >= n) break;
+#pragma unroll
+                for (int it = 0; it < ITC; ++it) {
+                    if (c < lim[it]) cp_async_16(tri + dst[it] + (L::lo_off(c) - L::lo_first(c)), src[it]);
+                    src[it] += lda;
                 }
-                cp_async_16(tri + gg * MS + pos, A0 + gg * sa + c * lda + Q * E);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < N; ++c) {
+                if (c >= n) break;
+#pragma unroll
+                for (int it = 0; it < ITC; ++it) {
+                    if (c >= lim[it]) cp_async_16(tri + dst[it] + L::up_off(c), src[it]);
+                    src[it] += lda;
+                }
             }
         }
     } else {
@@ -311,15 +328,16 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
             if (factor) {
                 const bool ok = d > Rt(0);
                 rs = ok ? rsqrt_of(d) : Rt(0);
-                const Rt ljj = ok ? d * rs : d;
                 failed |= ok ? 0u : (1u << j);
                 // scale rows >= j (rows < j of block rj are unused upper entries: scaling them
-                // is harmless), then put the diagonal
+                // is harmless). For a real type the diagonal comes out as d * (1/sqrt(d)) by the
+                // same scaling; a complex diagonal is set to that real value (its imaginary part
+                // is ignored). A failed pivot zeroes its column (the rest is unspecified).
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (r < rj) continue;
                     T v = scale(a[r][j], rs);
-                    if (r == rj && l == lj) v = from_real<T>(ljj);
+                    if (is_cplx<T>::value && r == rj && l == lj) v = from_real<T>(d * rs);
                     a[r][j] = v;
                     col[l + P * r] = v;
                 }
@@ -443,17 +461,22 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
                 }
         }
         if (!upper) {
+            // one running column pointer; a row block entirely at or below the diagonal needs
+            // only its rows' bounds check
             bool row_ok[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) row_ok[r] = live && (l + P * r < n);
+            T *Ac = A + l;
 #pragma unroll
-            for (int c = 0; c < N; ++c)
+            for (int c = 0; c < N; ++c) {
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (P * r + P - 1 < c) continue;
-                    const int i = l + P * r;
-                    if (row_ok[r] && i >= c) A[static_cast<int64_t>(c) * lda + i] = a[r][c];
+                    const bool below = P * r >= c || l + P * r >= c;
+                    if (row_ok[r] && below) Ac[P * r] = a[r][c];
                 }
+                Ac += lda;
+            }
         } else {
             // U(c,i) = conj(L(i,c)): column i of U is row i of L; transpose through the slab,
             // one block of P rows (= P columns of U) at a time
