@@ -59,9 +59,13 @@ typedef enum {
  *   info      device int32[batch]; receives 0 or the 1-based first failing column.
  *   stream    CUDA stream.
  *
- * Any alignment of A, lda and stride_a is accepted. For a failed item only info and the
- * leading (info-1) x (info-1) block of the factor are defined; the rest of the referenced
- * triangle holds unspecified finite or non-finite values.
+ * A must be aligned to its element size (4, 8, 8 or 16 bytes for f32, f64, c64, c128) and info
+ * to 4 bytes; lda and stride_a may take any value (16-byte aligned columns take faster copy
+ * paths). For a failed item only info and the leading (info-1) x (info-1) block of the factor
+ * are defined; the rest of the referenced triangle holds unspecified finite or non-finite
+ * values. info[b] = -1 reports that the kernel gave up waiting for an asynchronous copy or
+ * tensor-core operation of that item (a device fault, not a numerical result): the item's
+ * outputs are undefined.
  */
 bl_status bl_potrf(bl_uplo uplo, bl_dtype dtype, int64_t n, int64_t batch, void *A,
                    int64_t lda, int64_t stride_a, int32_t *info, bl_stream_t stream);
@@ -70,7 +74,8 @@ bl_status bl_potrf(bl_uplo uplo, bl_dtype dtype, int64_t n, int64_t batch, void 
  * bl_posv -- factor A as bl_potrf does, then solve A*X = B for nrhs right-hand sides per item
  * (forward substitution with L, back substitution with L^H; Upper uses U^H and U).
  *
- *   B         device pointer, n x nrhs per item, ldb >= n, stride_b >= ldb*nrhs. Overwritten
+ *   B         device pointer, n x nrhs per item, aligned to the element size, ldb >= n,
+ *             stride_b >= ldb*nrhs. Overwritten
  *             by X for items whose factorisation succeeded; left untouched for failed items.
  *   nrhs      nrhs >= 1. Any nrhs is accepted; the fused kernels take up to 8 (or fewer,
  *             depending on the kernel) per pass and larger counts run in further passes of the

@@ -15,6 +15,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdint>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -393,6 +394,11 @@ bl_status validate(int op, int uplo, int dtype, int64_t n, int64_t nrhs, int64_t
     if (batch < 1 || batch > kMaxBatch)
         return fail(BL_ERR_INVALID_ARGUMENT, "batch=%lld outside [1, %lld]", (long long)batch, (long long)kMaxBatch);
     if (A == nullptr) return fail(BL_ERR_INVALID_ARGUMENT, "A is NULL");
+    const size_t es = elem_size(dtype);
+    if (reinterpret_cast<uintptr_t>(A) % es != 0)
+        return fail(BL_ERR_INVALID_ARGUMENT, "A is not aligned to its %zu-byte element", es);
+    if (info != nullptr && reinterpret_cast<uintptr_t>(info) % 4 != 0)
+        return fail(BL_ERR_INVALID_ARGUMENT, "info is not 4-byte aligned");
     if (lda < n) return fail(BL_ERR_INVALID_ARGUMENT, "lda=%lld < n=%lld", (long long)lda, (long long)n);
     if (lda > INT64_MAX / n / 16) return fail(BL_ERR_INVALID_ARGUMENT, "lda=%lld too large", (long long)lda);
     if (stride_a < lda * n)
@@ -402,6 +408,8 @@ bl_status validate(int op, int uplo, int dtype, int64_t n, int64_t nrhs, int64_t
     if (op != OP_POTRF) {
         if (nrhs < 1 || nrhs > kMaxN) return fail(BL_ERR_INVALID_ARGUMENT, "nrhs=%lld outside [1, %lld]", (long long)nrhs, (long long)kMaxN);
         if (B == nullptr) return fail(BL_ERR_INVALID_ARGUMENT, "B is NULL");
+        if (reinterpret_cast<uintptr_t>(B) % es != 0)
+            return fail(BL_ERR_INVALID_ARGUMENT, "B is not aligned to its %zu-byte element", es);
         if (ldb < n) return fail(BL_ERR_INVALID_ARGUMENT, "ldb=%lld < n=%lld", (long long)ldb, (long long)n);
         if (ldb > INT64_MAX / nrhs / 16) return fail(BL_ERR_INVALID_ARGUMENT, "ldb=%lld too large", (long long)ldb);
         if (stride_b < ldb * nrhs)

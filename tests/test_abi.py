@@ -76,6 +76,10 @@ def test_invalid_pointers_strides_and_enums_are_rejected_without_a_gpu(bl):
     assert lib.bl_posv(0, 0, 4, 2, 1, fake, 4, 16, fake, 3, 8, fake, None) == 1  # ldb < n
     assert lib.bl_posv(0, 0, 4, 2, 2, fake, 4, 16, fake, 4, 7, fake, None) == 1  # B items overlap
     assert lib.bl_potrs(0, 0, 4, 0, 1, fake, 4, 16, fake, 4, 4, None) == 1      # nrhs 0
+    assert lib.bl_potrf(0, 1, 4, 1, fake + 4, 4, 16, fake, None) == 1       # f64 A not 8-aligned
+    assert lib.bl_potrf(0, 3, 4, 1, fake + 8, 4, 16, fake, None) == 1       # c128 A not 16-aligned
+    assert lib.bl_potrf(0, 0, 4, 1, fake, 4, 16, fake + 2, None) == 1       # info not 4-aligned
+    assert lib.bl_posv(0, 1, 4, 2, 1, fake, 4, 16, fake + 4, 4, 8, fake, None) == 1  # B not 8-aligned
     assert b"lda" in lib.bl_last_error() or lib.bl_last_error()
     assert lib.bl_set_route(b"getrf", b"tile:p=4:s=8") == 1
 
