@@ -2,6 +2,7 @@
 #pragma once
 
 #include <atomic>
+#include <cstdint>
 #include <cuda_runtime.h>
 
 #include "bl_types.cuh"
@@ -67,6 +68,19 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     const int64_t groups = (a.batch + C::G - 1) / C::G;
     const int64_t ctas = (groups + C::WARPS - 1) / C::WARPS;
     if (a.mode == MODE_POTRF) {
+        if constexpr (C::full_ok) {
+            // Lower items stored back to back (n = N, lda = N, stride = N*N, 16-byte aligned):
+            // each group is one contiguous run, copied whole into full-square slabs
+            if (!a.upper && a.n == C::N && a.lda == C::N && a.stride_a == static_cast<int64_t>(C::N) * C::N &&
+                (reinterpret_cast<uintptr_t>(a.A) & 15) == 0) {
+                auto kern = warp_kernel<T, P, R, false, C::min_blocks(), true>;
+                static std::atomic<unsigned long long> done{0};
+                cudaError_t e = ensure_smem(kern, C::smem_full, done);
+                if (e != cudaSuccess) return e;
+                kern<<<persistent_grid(kern, C::THREADS, C::smem_full, ctas), C::THREADS, C::smem_full, st>>>(a);
+                return cudaGetLastError();
+            }
+        }
         auto kern = warp_kernel<T, P, R, false, C::min_blocks()>;
         const size_t sm = a.upper ? C::smem_potrf : C::smem_lower;  // Lower needs no staging slab
         static std::atomic<unsigned long long> done{0};

@@ -112,6 +112,13 @@ struct WarpCfg {
     static constexpr size_t off_x = off_rs + (rs_bytes + 15) / 16 * 16;
     static constexpr size_t x_bytes = sizeof(T) * 2 * RB * SLOTS;
     static constexpr size_t smem_lower = off_stage;               // Lower potrf: no staging slab
+    // full-square slabs (Lower potrf of contiguous n = N items): each matrix copied whole, a
+    // 32-byte shift between matrices so the warp's partitions read disjoint banks
+    static constexpr int FSTRIDE = N * N + 32 / static_cast<int>(sizeof(T));
+    static constexpr size_t full_bytes = sizeof(T) * FSTRIDE * SLOTS;
+    static constexpr size_t off_col_full = (full_bytes + 15) / 16 * 16;
+    static constexpr size_t smem_full = off_col_full + (col_bytes + 15) / 16 * 16;
+    static constexpr bool full_ok = sizeof(T) == 4 && (N * N / E) % 32 == 0;
     static constexpr size_t smem_potrf = off_stage + stage_bytes;
     static constexpr size_t smem_solve = off_x + x_bytes;
     // launch bound for the factor-only kernel: registers held by the rows (32-bit words) plus
@@ -139,7 +146,7 @@ __device__ __forceinline__ int lower_slab_offset(int c) {
 // Lanes map to fixed (matrix, chunk) or (matrix, row) pairs and sweep the columns, so the copy
 // costs a handful of registers, not one address per chunk; 16-byte chunks when the layout
 // allows them, element copies otherwise.
-template <typename T, int P, int R>
+template <typename T, int P, int R, bool FULL = false>
 __device__ __forceinline__ void warp_prefetch(const BatchArgs &args, T *tri, int64_t grp, int lane, bool vec) {
     using C = WarpCfg<T, P, R>;
     constexpr int N = C::N, G = C::G, E = C::E, MS = C::MSTRIDE;
@@ -148,6 +155,22 @@ __device__ __forceinline__ void warp_prefetch(const BatchArgs &args, T *tri, int
     const bool upper = args.upper != 0;
     const T *A0 = static_cast<const T *>(args.A) + grp * G * sa;
     const int64_t mleft = args.batch - grp * G;            // live matrices in this group
+    if constexpr (FULL) {
+        // the group's items are one contiguous run of G*N*N elements: chunk k of it (16 bytes)
+        // goes to matrix k / (N*N/E) of the slab; every offset but the lane's is an immediate
+        constexpr int CPM = N * N / E;                     // chunks per matrix
+        constexpr int IT = G * CPM / 32;
+        static_assert((G * CPM) % 32 == 0 && CPM % 32 == 0, "whole chunks per lane");
+        const T *src = A0 + lane * E;
+        T *dst = tri + lane * E;
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int gg = (32 * it) / CPM;
+            if (gg < mleft) cp_async_16(dst + gg * C::FSTRIDE + (32 * it - gg * CPM) * E, src + 32 * it * E);
+        }
+        cp_async_commit();
+        return;
+    }
     if (vec) {
         // lanes map to fixed (matrix, 16-byte chunk) pairs; the column loop is unrolled so every
         // slab offset is a compile-time constant, the source is one running pointer per sweep,
@@ -214,7 +237,7 @@ __device__ __forceinline__ void warp_prefetch(const BatchArgs &args, T *tri, int
     cp_async_commit();
 }
 
-template <typename T, int P, int R, bool SOLVE, int MINB>
+template <typename T, int P, int R, bool SOLVE, int MINB, bool FULL = false>
 __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
     using C = WarpCfg<T, P, R>;
     using L = TriSlab<C::N, C::E>;
@@ -231,8 +254,9 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
     const int n = args.n;
     const bool upper = args.upper != 0;
     const int64_t lda_in = args.lda;
-    T *tri = reinterpret_cast<T *>(smem) + warp * G * MS;       // the warp's slab (G matrices)
-    T *colbuf = reinterpret_cast<T *>(smem + C::off_col) + slot * C::COLS;
+    // the warp's slab (G matrices): compacted triangles, or whole squares (FULL)
+    T *tri = reinterpret_cast<T *>(smem) + warp * G * (FULL ? C::FSTRIDE : MS);
+    T *colbuf = reinterpret_cast<T *>(smem + (FULL ? C::off_col_full : C::off_col)) + slot * C::COLS;
     T *stage = reinterpret_cast<T *>(smem + C::off_stage) + slot * P * LDU;
     const int mode = SOLVE ? args.mode : MODE_POTRF;
     const bool factor = mode != MODE_POTRS;
@@ -244,14 +268,17 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
     // so filling the whole slab with the identity once makes every later pick see an n x n item
     // bordered by the identity. The column loop then runs all N steps with no run-time bounds:
     // padding pivots are exactly 1 and padding entries stay 0.
-    for (int t = lane; t < G * MS; t += 32) tri[t] = zero<T>();
-    __syncwarp();
-    for (int t = lane; t < G * N; t += 32) {
-        const int gg = t / N, c = t - gg * N;
-        const int pos = upper ? upper_slab_offset(c, E) + c : lower_slab_offset<N, E>(c) + c - (c / E) * E;
-        tri[gg * MS + pos] = from_real<T>(Rt(1));
+    // (whole squares of n = N items need no padding)
+    if (!FULL) {
+        for (int t = lane; t < G * MS; t += 32) tri[t] = zero<T>();
+        __syncwarp();
+        for (int t = lane; t < G * N; t += 32) {
+            const int gg = t / N, c = t - gg * N;
+            const int pos = upper ? upper_slab_offset(c, E) + c : lower_slab_offset<N, E>(c) + c - (c / E) * E;
+            tri[gg * MS + pos] = from_real<T>(Rt(1));
+        }
+        __syncwarp();
     }
-    __syncwarp();
 
     // 16-byte chunk copies need every column start 16-byte aligned and whole chunks inside n
     const bool vec = (n % E == 0) && ((lda_in * static_cast<int64_t>(sizeof(T))) % 16 == 0) &&
@@ -260,7 +287,7 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
     const int64_t ngroups = (args.batch + G - 1) / G;
     const int64_t gstep = static_cast<int64_t>(gridDim.x) * C::WARPS;
     int64_t grp = static_cast<int64_t>(blockIdx.x) * C::WARPS + warp;
-    if (grp < ngroups) warp_prefetch<T, P, R>(args, tri, grp, lane, vec);
+    if (grp < ngroups) warp_prefetch<T, P, R, FULL>(args, tri, grp, lane, vec);
 
     for (; grp < ngroups; grp += gstep) {
         // Opaque copies of the lane index and leading dimension: without them the compiler
@@ -277,8 +304,16 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
         T a[R][N];
         cp_async_wait_all();
         __syncwarp();
-        const T *my = tri + g * MS;
-        if (!upper) {
+        const T *my = tri + g * (FULL ? C::FSTRIDE : MS);
+        if (FULL) {
+#pragma unroll
+            for (int c = 0; c < N; ++c)
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (P * r + P - 1 < c) continue;          // block r has no row >= c
+                    a[r][c] = my[c * N + l + P * r];
+                }
+        } else if (!upper) {
 #pragma unroll
             for (int c = 0; c < N; ++c)
 #pragma unroll
@@ -298,7 +333,7 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
             }
         }
         __syncwarp();
-        if (grp + gstep < ngroups) warp_prefetch<T, P, R>(args, tri, grp + gstep, lane, vec);
+        if (grp + gstep < ngroups) warp_prefetch<T, P, R, FULL>(args, tri, grp + gstep, lane, vec);
 
         T *A = static_cast<T *>(args.A) + (live ? mat * args.stride_a : 0);
         T *B = SOLVE ? static_cast<T *>(args.B) + (live ? mat * args.stride_b : 0) : nullptr;
