@@ -67,12 +67,13 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     using C = WarpCfg<T, P, R>;
     const int64_t groups = (a.batch + C::G - 1) / C::G;
     const int64_t ctas = (groups + C::WARPS - 1) / C::WARPS;
+    // Lower items stored back to back (n = N, lda = N, stride = N*N, 16-byte aligned): each group
+    // is one contiguous run, copied whole into full-square slabs
+    const bool full = !a.upper && a.n == C::N && a.lda == C::N &&
+                      a.stride_a == static_cast<int64_t>(C::N) * C::N && (reinterpret_cast<uintptr_t>(a.A) & 15) == 0;
     if (a.mode == MODE_POTRF) {
         if constexpr (C::full_ok) {
-            // Lower items stored back to back (n = N, lda = N, stride = N*N, 16-byte aligned):
-            // each group is one contiguous run, copied whole into full-square slabs
-            if (!a.upper && a.n == C::N && a.lda == C::N && a.stride_a == static_cast<int64_t>(C::N) * C::N &&
-                (reinterpret_cast<uintptr_t>(a.A) & 15) == 0) {
+            if (full) {
                 auto kern = warp_kernel<T, P, R, false, C::min_blocks(), true>;
                 static std::atomic<unsigned long long> done{0};
                 cudaError_t e = ensure_smem(kern, C::smem_full, done);
@@ -88,6 +89,16 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         kern<<<persistent_grid(kern, C::THREADS, sm, ctas), C::THREADS, sm, st>>>(a);
     } else {
+        if constexpr (C::full_ok && C::smem_solve_full <= 227 * 1024) {
+            if (full) {
+                auto kern = warp_kernel<T, P, R, true, 1, true>;
+                static std::atomic<unsigned long long> done{0};
+                cudaError_t e = ensure_smem(kern, C::smem_solve_full, done);
+                if (e != cudaSuccess) return e;
+                kern<<<persistent_grid(kern, C::THREADS, C::smem_solve_full, ctas), C::THREADS, C::smem_solve_full, st>>>(a);
+                return cudaGetLastError();
+            }
+        }
         auto kern = warp_kernel<T, P, R, true, 1>;
         static std::atomic<unsigned long long> done{0};
         cudaError_t e = ensure_smem(kern, C::smem_solve, done);

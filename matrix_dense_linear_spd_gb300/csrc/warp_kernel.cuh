@@ -121,6 +121,8 @@ struct WarpCfg {
     static constexpr bool full_ok = sizeof(T) == 4 && (N * N / E) % 32 == 0;
     static constexpr size_t smem_potrf = off_stage + stage_bytes;
     static constexpr size_t smem_solve = off_x + x_bytes;
+    static constexpr size_t full_shift = off_col_full - off_col;   // solve areas move up by this
+    static constexpr size_t smem_solve_full = smem_solve + full_shift;
     // launch bound for the factor-only kernel: registers held by the rows (32-bit words) plus
     // about 45 for addresses and temporaries, rounded down to whole CTAs per SM
     static constexpr int min_blocks() {
@@ -257,12 +259,13 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
     // the warp's slab (G matrices): compacted triangles, or whole squares (FULL)
     T *tri = reinterpret_cast<T *>(smem) + warp * G * (FULL ? C::FSTRIDE : MS);
     T *colbuf = reinterpret_cast<T *>(smem + (FULL ? C::off_col_full : C::off_col)) + slot * C::COLS;
-    T *stage = reinterpret_cast<T *>(smem + C::off_stage) + slot * P * LDU;
+    constexpr size_t shift = FULL ? C::full_shift : 0;
+    T *stage = reinterpret_cast<T *>(smem + C::off_stage + shift) + slot * P * LDU;
     const int mode = SOLVE ? args.mode : MODE_POTRF;
     const bool factor = mode != MODE_POTRS;
     const int nrhs = SOLVE ? min(args.nrhs, RHS) : 0;
-    Rt *rsb = SOLVE ? reinterpret_cast<Rt *>(smem + C::off_rs) + slot * N : nullptr;
-    T *xsb = SOLVE ? reinterpret_cast<T *>(smem + C::off_x) + slot * 2 * RB : nullptr;
+    Rt *rsb = SOLVE ? reinterpret_cast<Rt *>(smem + C::off_rs + shift) + slot * N : nullptr;
+    T *xsb = SOLVE ? reinterpret_cast<T *>(smem + C::off_x + shift) + slot * 2 * RB : nullptr;
 
     // Identity padding: the slab positions of rows/columns >= n are never written by a prefetch,
     // so filling the whole slab with the identity once makes every later pick see an n x n item
