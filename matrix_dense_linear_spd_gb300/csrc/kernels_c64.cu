@@ -9,10 +9,14 @@ static const KernelEntry k_entries_c64[] = {
     warp_entry<cf32, 4, 2>(),
     warp_entry<cf32, 8, 1>(),
     warp_entry<cf32, 4, 4>(),
+    warp_entry<cf32, 4, 4, true>(),
     warp_entry<cf32, 8, 2>(),
+    warp_entry<cf32, 8, 2, true>(),
     warp_entry<cf32, 16, 1>(),
     warp_entry<cf32, 8, 3>(),
+    warp_entry<cf32, 8, 3, true>(),
     warp_entry<cf32, 16, 2>(),
+    warp_entry<cf32, 16, 2, true>(),
     warp_entry<cf32, 32, 1>(),
     tile_entry<cf32, 2, 2>(),
     tile_entry<cf32, 2, 4>(),

@@ -9,12 +9,17 @@ static const KernelEntry k_entries_f32[] = {
     warp_entry<float, 4, 2>(),
     warp_entry<float, 8, 1>(),
     warp_entry<float, 4, 4>(),
+    warp_entry<float, 4, 4, true>(),
     warp_entry<float, 8, 2>(),
+    warp_entry<float, 8, 2, true>(),
     warp_entry<float, 16, 1>(),
     warp_entry<float, 8, 3>(),
     warp_entry<float, 4, 8>(),
+    warp_entry<float, 4, 8, true>(),
     warp_entry<float, 8, 4>(),
+    warp_entry<float, 8, 4, true>(),
     warp_entry<float, 16, 2>(),
+    warp_entry<float, 16, 2, true>(),
     warp_entry<float, 32, 1>(),
     tile_entry<float, 2, 2>(),
     tile_entry<float, 2, 4>(),

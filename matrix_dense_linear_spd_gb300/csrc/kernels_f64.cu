@@ -12,10 +12,14 @@ static const KernelEntry k_entries_f64[] = {
     warp_entry<double, 4, 2>(),
     warp_entry<double, 8, 1>(),
     warp_entry<double, 4, 4>(),
+    warp_entry<double, 4, 4, true>(),
     warp_entry<double, 8, 2>(),
+    warp_entry<double, 8, 2, true>(),
     warp_entry<double, 16, 1>(),
     warp_entry<double, 8, 3>(),
+    warp_entry<double, 8, 3, true>(),
     warp_entry<double, 8, 4>(),
+    warp_entry<double, 8, 4, true>(),
     warp_entry<double, 16, 2>(),
     warp_entry<double, 32, 1>(),
     tile_entry<double, 2, 2>(),

@@ -62,17 +62,20 @@ inline unsigned persistent_grid(K kern, int threads, size_t smem, int64_t ctas_n
     return static_cast<unsigned>(ctas_needed < full ? ctas_needed : full);
 }
 
-template <typename T, int P, int R>
+// WHOLE: the "full=1" variant, which copies whole squares into its slabs when the call's items are
+// stored back to back (Lower, n = N, lda = N, stride = N*N, 16-byte aligned) and otherwise runs the
+// compacted-triangle kernel like the plain variant (same arithmetic, bit-identical results).
+template <typename T, int P, int R, bool WHOLE = false>
 cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     using C = WarpCfg<T, P, R>;
     const int64_t groups = (a.batch + C::G - 1) / C::G;
     const int64_t ctas = (groups + C::WARPS - 1) / C::WARPS;
     // Lower items stored back to back (n = N, lda = N, stride = N*N, 16-byte aligned): each group
     // is one contiguous run, copied whole into full-square slabs
-    const bool full = !a.upper && a.n == C::N && a.lda == C::N &&
+    const bool full = WHOLE && !a.upper && a.n == C::N && a.lda == C::N &&
                       a.stride_a == static_cast<int64_t>(C::N) * C::N && (reinterpret_cast<uintptr_t>(a.A) & 15) == 0;
     if (a.mode == MODE_POTRF) {
-        if constexpr (C::full_ok) {
+        if constexpr (WHOLE && C::full_ok) {
             if (full) {
                 auto kern = warp_kernel<T, P, R, false, C::min_blocks(), true>;
                 static std::atomic<unsigned long long> done{0};
@@ -89,7 +92,7 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         kern<<<persistent_grid(kern, C::THREADS, sm, ctas), C::THREADS, sm, st>>>(a);
     } else {
-        if constexpr (C::full_ok && C::smem_solve_full <= 227 * 1024) {
+        if constexpr (WHOLE && C::full_ok && C::smem_solve_full <= 227 * 1024) {
             if (full) {
                 auto kern = warp_kernel<T, P, R, true, 1, true>;
                 static std::atomic<unsigned long long> done{0};
@@ -108,10 +111,12 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <typename T, int P, int R>
+template <typename T, int P, int R, bool WHOLE = false>
 constexpr KernelEntry warp_entry() {
     using C = WarpCfg<T, P, R>;
-    return KernelEntry{2, P, R, 0, C::N, C::RHS, C::THREADS, C::PER_CTA, C::smem_solve, &launch_warp<T, P, R>};
+    static_assert(!WHOLE || C::full_ok, "whole-square slabs need whole 16-byte chunks per lane");
+    return KernelEntry{2, P, R, WHOLE ? 1 : 0, C::N, C::RHS, C::THREADS, C::PER_CTA,
+                       WHOLE ? C::smem_solve_full : C::smem_solve, &launch_warp<T, P, R, WHOLE>};
 }
 
 template <typename T, int NMAX>

@@ -112,13 +112,14 @@ struct WarpCfg {
     static constexpr size_t off_x = off_rs + (rs_bytes + 15) / 16 * 16;
     static constexpr size_t x_bytes = sizeof(T) * 2 * RB * SLOTS;
     static constexpr size_t smem_lower = off_stage;               // Lower potrf: no staging slab
-    // full-square slabs (Lower potrf of contiguous n = N items): each matrix copied whole, a
-    // 32-byte shift between matrices so the warp's partitions read disjoint banks
-    static constexpr int FSTRIDE = N * N + 32 / static_cast<int>(sizeof(T));
+    // full-square slabs (Lower items stored back to back, n = N): each matrix copied whole, a
+    // shift of P elements between matrices so the warp's partitions read disjoint banks
+    static constexpr int FSTRIDE = N * N + P;
     static constexpr size_t full_bytes = sizeof(T) * FSTRIDE * SLOTS;
     static constexpr size_t off_col_full = (full_bytes + 15) / 16 * 16;
     static constexpr size_t smem_full = off_col_full + (col_bytes + 15) / 16 * 16;
-    static constexpr bool full_ok = sizeof(T) == 4 && (N * N / E) % 32 == 0;
+    static constexpr bool full_ok = sizeof(T) <= 8 && (N * N / E) % 32 == 0 && (P * sizeof(T)) % 16 == 0 &&
+                                    (N * N * sizeof(T)) % 128 == 0;
     static constexpr size_t smem_potrf = off_stage + stage_bytes;
     static constexpr size_t smem_solve = off_x + x_bytes;
     static constexpr size_t full_shift = off_col_full - off_col;   // solve areas move up by this
