@@ -1,5 +1,6 @@
 """Per-workload report: every named synthetic workload measured with the benchmark protocol
-(input restored and L2 flushed before each call, CUDA events around the call), with
+(input restored and L2 flushed before each call, CUDA events around the call, trimmed mean
+of the middle 60% of the repetitions), with
 matrices/s, GB/s, GFLOP/s and the achieved fraction of the binding roof, next to cuSOLVER's
 batched potrf (through torch.linalg.cholesky_ex) as a reference point.
 
@@ -109,7 +110,9 @@ def main(argv=None):
                 torch.cuda.synchronize()
                 if it >= 3:
                     ts.append(e0.elapsed_time(e1))
-            ms = statistics.median(ts)
+            ts.sort()
+            k = len(ts) // 5
+            ms = statistics.mean(ts[k:len(ts) - k] or ts)
             route = bl.last_choice()
             expect = w.planted_info if w.planted_info is not None else np.zeros(batch, np.int32)
             ok = np.array_equal(info.cpu().numpy(), expect)
@@ -138,7 +141,9 @@ def main(argv=None):
                     torch.cuda.synchronize()
                     if it >= 2:
                         vt.append(e0.elapsed_time(e1))
-                vms = statistics.median(vt)
+                vt.sort()
+                k = len(vt) // 5
+                vms = statistics.mean(vt[k:len(vt) - k] or vt)
                 vend = f"{vms:.4f}"
                 ratio = f"{vms / ms:.1f}"
             flag = "" if ok else " (info MISMATCH)"
