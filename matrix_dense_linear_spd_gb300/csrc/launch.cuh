@@ -63,25 +63,26 @@ inline unsigned persistent_grid(K kern, int threads, size_t smem, int64_t ctas_n
 }
 
 // WHOLE: the "full=1" variant, which copies whole squares into its slabs when the call's items are
-// stored back to back (Lower, n = N, lda = N, stride = N*N, 16-byte aligned) and otherwise runs the
+// stored back to back (n = N, lda = N, stride = N*N, 16-byte aligned) and otherwise runs the
 // compacted-triangle kernel like the plain variant (same arithmetic, bit-identical results).
 template <typename T, int P, int R, bool WHOLE = false>
 cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     using C = WarpCfg<T, P, R>;
     const int64_t groups = (a.batch + C::G - 1) / C::G;
     const int64_t ctas = (groups + C::WARPS - 1) / C::WARPS;
-    // Lower items stored back to back (n = N, lda = N, stride = N*N, 16-byte aligned): each group
-    // is one contiguous run, copied whole into full-square slabs
-    const bool full = WHOLE && !a.upper && a.n == C::N && a.lda == C::N &&
+    // items stored back to back (n = N, lda = N, stride = N*N, 16-byte aligned): each group is one
+    // contiguous run, copied whole into full-square slabs
+    const bool full = WHOLE && a.n == C::N && a.lda == C::N &&
                       a.stride_a == static_cast<int64_t>(C::N) * C::N && (reinterpret_cast<uintptr_t>(a.A) & 15) == 0;
     if (a.mode == MODE_POTRF) {
         if constexpr (WHOLE && C::full_ok) {
             if (full) {
                 auto kern = warp_kernel<T, P, R, false, C::min_blocks(), true>;
+                const size_t sm = a.upper ? C::smem_potrf_full : C::smem_full;   // Upper stages its store
                 static std::atomic<unsigned long long> done{0};
-                cudaError_t e = ensure_smem(kern, C::smem_full, done);
+                cudaError_t e = ensure_smem(kern, C::smem_potrf_full, done);
                 if (e != cudaSuccess) return e;
-                kern<<<persistent_grid(kern, C::THREADS, C::smem_full, ctas), C::THREADS, C::smem_full, st>>>(a);
+                kern<<<persistent_grid(kern, C::THREADS, sm, ctas), C::THREADS, sm, st>>>(a);
                 return cudaGetLastError();
             }
         }

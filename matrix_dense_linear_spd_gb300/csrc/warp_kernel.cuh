@@ -112,18 +112,24 @@ struct WarpCfg {
     static constexpr size_t off_x = off_rs + (rs_bytes + 15) / 16 * 16;
     static constexpr size_t x_bytes = sizeof(T) * 2 * RB * SLOTS;
     static constexpr size_t smem_lower = off_stage;               // Lower potrf: no staging slab
-    // full-square slabs (Lower items stored back to back, n = N): each matrix copied whole, a
-    // shift of P elements between matrices so the warp's partitions read disjoint banks
-    static constexpr int FSTRIDE = N * N + P;
+    // full-square slabs (items stored back to back, n = N): each matrix copied whole. Lower keeps
+    // the column stride N (the copy is one contiguous run per matrix); Upper pads each column by
+    // 16 bytes so a row of S (a column of A) reads in 16-byte pieces across 8 lanes without bank
+    // conflicts. The matrix stride is congruent to P modulo one bank cycle (the warp's
+    // partitions read disjoint banks).
+    static constexpr int NS_L = N;
+    static constexpr int NS = N + E;
+    static constexpr int FSTRIDE = N * NS + ((P - (N * NS) % BANKCYC) % BANKCYC + BANKCYC) % BANKCYC;
     static constexpr size_t full_bytes = sizeof(T) * FSTRIDE * SLOTS;
     static constexpr size_t off_col_full = (full_bytes + 15) / 16 * 16;
     static constexpr size_t smem_full = off_col_full + (col_bytes + 15) / 16 * 16;
     static constexpr bool full_ok = sizeof(T) <= 8 && (N * N / E) % 32 == 0 && (P * sizeof(T)) % 16 == 0 &&
-                                    (N * N * sizeof(T)) % 128 == 0;
+                                    (FSTRIDE * sizeof(T)) % 16 == 0;
     static constexpr size_t smem_potrf = off_stage + stage_bytes;
     static constexpr size_t smem_solve = off_x + x_bytes;
     static constexpr size_t full_shift = off_col_full - off_col;   // solve areas move up by this
     static constexpr size_t smem_solve_full = smem_solve + full_shift;
+    static constexpr size_t smem_potrf_full = smem_potrf + full_shift;   // Upper: with the staging slab
     // launch bound for the factor-only kernel: registers held by the rows (32-bit words) plus
     // about 45 for addresses and temporaries, rounded down to whole CTAs per SM
     static constexpr int min_blocks() {
@@ -145,6 +151,29 @@ __device__ __forceinline__ int lower_slab_offset(int c) {
     return c * N - E * (E * m * (m - 1) / 2 + m * r);
 }
 
+// Copy one group's contiguous run of whole squares into the slab with column stride NS: chunk k
+// (16 bytes) is matrix k / CPM, column (k mod CPM) / CPCOL, chunk k mod CPCOL of that column.
+// When 32 lanes span whole columns every offset but the lane's is an immediate.
+template <typename T, int NS, int CPM, int CPCOL, int IT, int FSTRIDE, int E>
+__device__ __forceinline__ void full_copy(T *tri, const T *src, int lane, int64_t mleft) {
+    if constexpr (32 % CPCOL == 0) {
+        T *dst = tri + (lane / CPCOL) * NS + (lane % CPCOL) * E;
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int gg = (32 * it) / CPM;
+            const int c0 = (32 * it - gg * CPM) / CPCOL;
+            if (gg < mleft) cp_async_16(dst + gg * FSTRIDE + c0 * NS, src + 32 * it * E);
+        }
+    } else {
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int k = lane + 32 * it;
+            const int gg = k / CPM, w = k - gg * CPM, c = w / CPCOL, q = w - c * CPCOL;
+            if (gg < mleft) cp_async_16(tri + gg * FSTRIDE + c * NS + q * E, src + 32 * it * E);
+        }
+    }
+}
+
 // Issue the asynchronous copy of group `grp`'s referenced triangles into the warp's slab.
 // Lanes map to fixed (matrix, chunk) or (matrix, row) pairs and sweep the columns, so the copy
 // costs a handful of registers, not one address per chunk; 16-byte chunks when the layout
@@ -159,18 +188,14 @@ __device__ __forceinline__ void warp_prefetch(const BatchArgs &args, T *tri, int
     const T *A0 = static_cast<const T *>(args.A) + grp * G * sa;
     const int64_t mleft = args.batch - grp * G;            // live matrices in this group
     if constexpr (FULL) {
-        // the group's items are one contiguous run of G*N*N elements: chunk k of it (16 bytes)
-        // goes to matrix k / (N*N/E) of the slab; every offset but the lane's is an immediate
+        // the group's items are one contiguous run of G*N*N elements
         constexpr int CPM = N * N / E;                     // chunks per matrix
+        constexpr int CPCOL = N / E;                       // chunks per column
         constexpr int IT = G * CPM / 32;
         static_assert((G * CPM) % 32 == 0 && CPM % 32 == 0, "whole chunks per lane");
         const T *src = A0 + lane * E;
-        T *dst = tri + lane * E;
-#pragma unroll
-        for (int it = 0; it < IT; ++it) {
-            const int gg = (32 * it) / CPM;
-            if (gg < mleft) cp_async_16(dst + gg * C::FSTRIDE + (32 * it - gg * CPM) * E, src + 32 * it * E);
-        }
+        if (upper) full_copy<T, C::NS, CPM, CPCOL, IT, C::FSTRIDE, E>(tri, src, lane, mleft);
+        else full_copy<T, C::NS_L, CPM, CPCOL, IT, C::FSTRIDE, E>(tri, src, lane, mleft);
         cp_async_commit();
         return;
     }
@@ -309,14 +334,26 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
         cp_async_wait_all();
         __syncwarp();
         const T *my = tri + g * (FULL ? C::FSTRIDE : MS);
-        if (FULL) {
+        if (FULL && !upper) {
 #pragma unroll
             for (int c = 0; c < N; ++c)
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (P * r + P - 1 < c) continue;          // block r has no row >= c
-                    a[r][c] = my[c * N + l + P * r];
+                    a[r][c] = my[c * C::NS_L + l + P * r];
                 }
+        } else if (FULL) {
+            // row i of S is column i of A: 16 bytes at a time, conjugated
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const T *rowp = my + (l + P * r) * C::NS;
+#pragma unroll
+                for (int c = 0; c < P * r + P; c += E) {
+                    const Vec16<T> v = *reinterpret_cast<const Vec16<T> *>(rowp + c);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) a[r][c + e] = conj(v.v[e]);
+                }
+            }
         } else if (!upper) {
 #pragma unroll
             for (int c = 0; c < N; ++c)
