@@ -75,8 +75,8 @@ std::vector<const KernelEntry *> candidates(int dtype) {
 std::string spelling(const KernelEntry &e) {
     char buf[64];
     if (e.family == 0) snprintf(buf, sizeof buf, "tile:p=%d:s=%d", e.p, e.s);
-    else if (e.family == 2 && e.nb) snprintf(buf, sizeof buf, "warp:p=%d:r=%d:full=1", e.p, e.s);  // whole squares
-    else if (e.family == 2) snprintf(buf, sizeof buf, "warp:p=%d:r=%d", e.p, e.s);
+    else if (e.family == 2)   // nb bit 0: whole squares, bit 1: packed f32x2 update
+        snprintf(buf, sizeof buf, "warp:p=%d:r=%d%s%s", e.p, e.s, (e.nb & 1) ? ":full=1" : "", (e.nb & 2) ? ":x2=1" : "");
     else if (e.family == 3) snprintf(buf, sizeof buf, "thread:n=%d", e.nb);
     else if (e.s) snprintf(buf, sizeof buf, "blocked:nb=%d:tc=1", e.nb);   // tensor-core trailing update
     else snprintf(buf, sizeof buf, "blocked:nb=%d", e.nb);
@@ -97,7 +97,7 @@ std::string canon(std::string s) {
     while (std::getline(ss, tok, ':')) parts.push_back(tok);
     if (parts.empty()) return s;
     static const std::map<std::string, std::vector<std::string>> fields = {
-        {"tile", {"p", "s"}}, {"warp", {"p", "r", "full"}}, {"blocked", {"nb", "tc"}}, {"thread", {"n"}}};
+        {"tile", {"p", "s"}}, {"warp", {"p", "r", "full", "x2"}}, {"blocked", {"nb", "tc"}}, {"thread", {"n"}}};
     auto it = fields.find(parts[0]);
     if (it == fields.end()) return s;
     std::string out = parts[0];

@@ -65,7 +65,8 @@ inline unsigned persistent_grid(K kern, int threads, size_t smem, int64_t ctas_n
 // WHOLE: the "full=1" variant, which copies whole squares into its slabs when the call's items are
 // stored back to back (n = N, lda = N, stride = N*N, 16-byte aligned) and otherwise runs the
 // compacted-triangle kernel like the plain variant (same arithmetic, bit-identical results).
-template <typename T, int P, int R, bool WHOLE = false>
+// PK: packed two-lane FP32 FMAs in the factor-only kernel (f32; the solve kernel is shared).
+template <typename T, int P, int R, bool WHOLE = false, bool PK = false>
 cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     using C = WarpCfg<T, P, R>;
     const int64_t groups = (a.batch + C::G - 1) / C::G;
@@ -77,7 +78,7 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     if (a.mode == MODE_POTRF) {
         if constexpr (WHOLE && C::full_ok) {
             if (full) {
-                auto kern = warp_kernel<T, P, R, false, C::min_blocks(), true>;
+                auto kern = warp_kernel<T, P, R, false, PK ? C::min_blocks_packed() : C::min_blocks(), true, PK>;
                 const size_t sm = a.upper ? C::smem_potrf_full : C::smem_full;   // Upper stages its store
                 static std::atomic<unsigned long long> done{0};
                 cudaError_t e = ensure_smem(kern, C::smem_potrf_full, done);
@@ -86,7 +87,7 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
                 return cudaGetLastError();
             }
         }
-        auto kern = warp_kernel<T, P, R, false, C::min_blocks()>;
+        auto kern = warp_kernel<T, P, R, false, PK ? C::min_blocks_packed() : C::min_blocks(), false, PK>;
         const size_t sm = a.upper ? C::smem_potrf : C::smem_lower;  // Lower needs no staging slab
         static std::atomic<unsigned long long> done{0};
         cudaError_t e = ensure_smem(kern, C::smem_potrf, done);
@@ -112,12 +113,12 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <typename T, int P, int R, bool WHOLE = false>
+template <typename T, int P, int R, bool WHOLE = false, bool PK = false>
 constexpr KernelEntry warp_entry() {
     using C = WarpCfg<T, P, R>;
     static_assert(!WHOLE || C::full_ok, "whole-square slabs need whole 16-byte chunks per lane");
-    return KernelEntry{2, P, R, WHOLE ? 1 : 0, C::N, C::RHS, C::THREADS, C::PER_CTA,
-                       WHOLE ? C::smem_solve_full : C::smem_solve, &launch_warp<T, P, R, WHOLE>};
+    return KernelEntry{2, P, R, (WHOLE ? 1 : 0) | (PK ? 2 : 0), C::N, C::RHS, C::THREADS, C::PER_CTA,
+                       WHOLE ? C::smem_solve_full : C::smem_solve, &launch_warp<T, P, R, WHOLE, PK>};
 }
 
 template <typename T, int NMAX>

@@ -12,8 +12,8 @@ namespace bl {
 // right-hand sides one pass solves (0: any; -1: the variant does not solve).
 struct KernelEntry {
     int family;          // 0 = tile, 1 = blocked, 2 = warp, 3 = thread (potrf only)
-    int p, s, nb;        // tile geometry (p, s), warp geometry (p lanes, s = rows per lane; nb = 1:
-                         // whole-square slabs), blocked panel width nb (s = 1: tensor-core
+    int p, s, nb;        // tile geometry (p, s), warp geometry (p lanes, s = rows per lane; nb bit 0:
+                         // whole-square slabs, bit 1: packed f32x2 update), blocked panel width nb (s = 1: tensor-core
                          // trailing update), or thread capacity nb
     int cap;
     int rhs_max;

@@ -136,6 +136,11 @@ struct WarpCfg {
         const int m = 65536 / (THREADS * (row_words() + 45));
         return m < 1 ? 1 : (m > 8 ? 8 : m);
     }
+    // the packed update keeps column pairs in aligned register pairs: about 15 more per lane
+    static constexpr int min_blocks_packed() {
+        const int m = 65536 / (THREADS * (row_words() + 60));
+        return m < 1 ? 1 : (m > 8 ? 8 : m);
+    }
 };
 
 template <typename T>
@@ -265,8 +270,11 @@ __device__ __forceinline__ void warp_prefetch(const BatchArgs &args, T *tri, int
     cp_async_commit();
 }
 
-template <typename T, int P, int R, bool SOLVE, int MINB, bool FULL = false>
+// PK (f32 only): the rank-1 update runs on column pairs (k, k+1) as packed two-lane FP32 FMAs
+// (fma.rn.f32x2), one instruction per pair of entries of a row.
+template <typename T, int P, int R, bool SOLVE, int MINB, bool FULL = false, bool PK = false>
 __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
+    static_assert(!PK || (sizeof(T) == 4 && !is_cplx<T>::value && P % 2 == 0), "packed update: f32, even P");
     using C = WarpCfg<T, P, R>;
     using L = TriSlab<C::N, C::E>;
     using Rt = real_t<T>;
@@ -450,18 +458,47 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
                 }
             }
             if (!factor) continue;
-            // rank-1 update of the trailing rows/columns k > j, 16 bytes of the column at a time
+            if constexpr (PK) {
+                // pairs (k, k+1), k even: both trailing -> one packed FMA; only k+1 trailing (k = j)
+                // -> one scalar FMA. P is even, so a block with a row >= k also has one >= k+1.
+                float2 m2[R];
 #pragma unroll
-            for (int q = (j + 1) / E; q < CB / E; ++q) {
-                const Vec16<T> ck = reinterpret_cast<const Vec16<T> *>(col)[q];
+                for (int r = 0; r < R; ++r) m2[r] = make_float2(-re(a[r][j]), -re(a[r][j]));
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const int k = q * E + e;
-                    if (k <= j) continue;
+                for (int q = (j + 1) / E; q < CB / E; ++q) {
+                    const Vec16<T> ck = reinterpret_cast<const Vec16<T> *>(col)[q];
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        if (P * r + P - 1 < k) continue;   // no row >= k in block r
-                        sub_mul_conj(a[r][k], a[r][j], ck.v[e]);
+                    for (int e = 0; e < E; e += 2) {
+                        const int k = q * E + e;
+                        if (k + 1 <= j) continue;
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            if (P * r + P - 1 < k) continue;   // no row >= k in block r
+                            if (k <= j) {
+                                sub_mul_conj(a[r][k + 1], a[r][j], ck.v[e + 1]);
+                            } else {
+                                const float2 t = __ffma2_rn(m2[r], make_float2(re(ck.v[e]), re(ck.v[e + 1])),
+                                                            make_float2(re(a[r][k]), re(a[r][k + 1])));
+                                a[r][k] = t.x;
+                                a[r][k + 1] = t.y;
+                            }
+                        }
+                    }
+                }
+            } else {
+                // rank-1 update of the trailing rows/columns k > j, 16 bytes of the column at a time
+#pragma unroll
+                for (int q = (j + 1) / E; q < CB / E; ++q) {
+                    const Vec16<T> ck = reinterpret_cast<const Vec16<T> *>(col)[q];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const int k = q * E + e;
+                        if (k <= j) continue;
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            if (P * r + P - 1 < k) continue;   // no row >= k in block r
+                            sub_mul_conj(a[r][k], a[r][j], ck.v[e]);
+                        }
                     }
                 }
             }
