@@ -1,0 +1,377 @@
+// Column-block tensor-core Cholesky ("blocked:nb=32:tc=2"), f32, n <= 512: one CTA per matrix,
+// the current block of 128 columns held as f32 accumulators in tensor memory.
+//
+// Method (BatchLAS "Batched Cholesky (potrf)" page, section "The blocked driver": factor the
+// diagonal block, solve the panel below it, update the rest; the update is the only dense
+// contraction). The columns are taken in blocks of W = 128; for the block C0 .. C0+W-1, whose
+// lower part has M = n - C0 rows:
+//   1. block update on the tensor cores, left-looking: D = L(C0:n, 0:C0) * L(C0:C0+W, 0:C0)^T,
+//      K in chunks of 32 columns of L. Each chunk is read once from global memory, split into
+//      tf32 hi and lo parts (3xTF32: hi*hi + hi*lo + lo*hi keeps f32 accuracy) and stored as a
+//      128-byte-swizzled K-major operand panel; the B operand is the panel's first W rows.
+//      D lives in tensor memory, one 128 x W tile per 128 rows (4 tiles = all 512 columns).
+//   2. the block column is factored right-looking, 32 columns (one slice) at a time. The slice's
+//      current values are S(:, slice) - D(:, slice): original values from global memory minus
+//      the accumulator read back with tcgen05.ld. One warp factors the 32 x 32 diagonal block in
+//      registers (pivot and column entries by shuffles; first non-positive pivot fails the item);
+//      every thread then solves its rows against it (L21 = A21 * L11^-T) and writes them to
+//      global memory. When the block has further slices, the solved rows are split into the
+//      operand panel and the tensor cores add L21 * L21^T to D for the block's remaining columns.
+// Each element of the referenced triangle is read from global memory once as input and written
+// once; later blocks read finished L columns (from L2) as operands.
+//
+// Upper runs on the view S(i,k) = A(k,i) (real type: no conjugation); only the referenced
+// triangle is ever written. A failure at column c reports info = c + 1 and the item stops (the
+// columns before c are final). Every wait on the tensor cores is bounded; a wait that gives up
+// reports info = -1.
+#pragma once
+
+#include "bl_types.cuh"
+#include "tc_sm100.cuh"
+
+namespace bl {
+
+struct ColBlkCfg {
+    static constexpr int THREADS = 256;
+    static constexpr int W = 128;                                   // block width (accumulator columns)
+    static constexpr int MAXN = 512;                                // 4 row tiles x 128 tensor-memory columns
+    // operand panels: rows x 32 tf32 (128 bytes), hi and lo parts. Panel 0 holds up to MAXN rows
+    // (the slices of the first block); panel 1, the second buffer of the block update, up to
+    // MAXN - W rows (blocks after the first). The diagonal block's L columns and reciprocal
+    // pivots live in panel 1's space: the slices never use panel 1.
+    static constexpr size_t P0_HI = 0;
+    static constexpr size_t P0_LO = static_cast<size_t>(MAXN) * 128;
+    static constexpr size_t P1_HI = 2 * P0_LO;
+    static constexpr size_t P1_LO = P1_HI + static_cast<size_t>(MAXN - W) * 128;
+    static constexpr size_t OFF_L11 = P1_HI;                        // sLs[c*32 + m] = L(c+m, c)
+    static constexpr size_t OFF_RS = OFF_L11 + 32 * 32 * 4;         // 1 / L(c, c)
+    static constexpr size_t END = P1_LO + static_cast<size_t>(MAXN - W) * 128;
+    static constexpr size_t smem_bytes = 1024 + END;                // + 1024 for the panel alignment
+    static_assert(OFF_RS + 32 * 4 <= END, "diagonal-block area inside panel 1");
+};
+
+namespace colblk {
+
+// Offset of S(i, k) in the stored matrix: Lower S = A, Upper S(i,k) = A(k,i).
+template <bool UPPER>
+__device__ __forceinline__ int64_t sidx(int i, int k, int64_t lda) {
+    return UPPER ? static_cast<int64_t>(i) * lda + k : static_cast<int64_t>(k) * lda + i;
+}
+
+// S(i, k0 + c) for c < 32 into v; entries with k0 + c >= kend are 0 (kend <= k0: all 0).
+template <bool UPPER>
+__device__ __forceinline__ void load_row(const float *A, int64_t lda, int i, int k0, int kend, float (&v)[32]) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] = (k0 + c < kend) ? A[sidx<UPPER>(i, k0 + c, lda)] : 0.f;
+}
+
+// Row `row` of the operand panel: the 32 values split into tf32 hi and lo parts, 16-byte chunks
+// at their 128-byte-swizzle positions.
+__device__ __forceinline__ void panel_row(unsigned char *hi, unsigned char *lo, int row, const float (&x)[32]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        float4 h4, l4;
+        tc::split_tf32(x[4 * q + 0], h4.x, l4.x);
+        tc::split_tf32(x[4 * q + 1], h4.y, l4.y);
+        tc::split_tf32(x[4 * q + 2], h4.z, l4.z);
+        tc::split_tf32(x[4 * q + 3], h4.w, l4.w);
+        const uint32_t off = tc::sw128_offset(row, 4 * q);
+        *reinterpret_cast<float4 *>(hi + off) = h4;
+        *reinterpret_cast<float4 *>(lo + off) = l4;
+    }
+}
+
+// One element of a panel row: its tf32 hi and lo parts at (row, k).
+__device__ __forceinline__ void panel_elem(unsigned char *hi, unsigned char *lo, int row, int k, float x) {
+    float h, l;
+    tc::split_tf32(x, h, l);
+    const uint32_t off = tc::sw128_offset(row, k);
+    *reinterpret_cast<float *>(hi + off) = h;
+    *reinterpret_cast<float *>(lo + off) = l;
+}
+
+// D[:, 0:N) (+)= A * B^T over K = 32 with the 3xTF32 split: A = panel rows [a_row0, a_row0 + 128),
+// B = panel rows [b_row0, b_row0 + N). `acc` false overwrites D on the first product.
+__device__ __forceinline__ void mma_chunk(uint32_t d, uint32_t s_hi, uint32_t s_lo, int a_row0, int b_row0, int N,
+                                          bool acc) {
+    const uint32_t idesc = tc::idesc_tf32(128, N);
+    const uint32_t ah = s_hi + static_cast<uint32_t>(a_row0) * 128u, al = s_lo + static_cast<uint32_t>(a_row0) * 128u;
+    const uint32_t bh = s_hi + static_cast<uint32_t>(b_row0) * 128u, bl_ = s_lo + static_cast<uint32_t>(b_row0) * 128u;
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+        tc::mma_tf32(d, tc::sdesc_sw128(ah + 32 * st), tc::sdesc_sw128(bh + 32 * st), idesc, acc || st > 0);
+        tc::mma_tf32(d, tc::sdesc_sw128(ah + 32 * st), tc::sdesc_sw128(bl_ + 32 * st), idesc, true);
+        tc::mma_tf32(d, tc::sdesc_sw128(al + 32 * st), tc::sdesc_sw128(bh + 32 * st), idesc, true);
+    }
+}
+
+// Factor the 32 x 32 diagonal block held by one warp (lane = row; padding rows are identity),
+// right-looking, one column per step in a compact loop: the lane's row is kept in a shifting
+// frame (a[0] is always the current column), so every register index is static and the loop
+// body stays small enough for the instruction cache. Column j of L is published to sLs[j*32 + m]
+// = L(j+m, j) (m = 0 is the diagonal), 1/L(j,j) to sRs[j]; the update reads the column back as
+// 16-byte broadcasts (positions past the block hold stale values and only touch entries past
+// the block). Returns the failure bit mask.
+__device__ __forceinline__ unsigned factor_diag(float (&a)[32], int lane, int kq, float *sLs, float *sRs) {
+    unsigned failed = 0;
+#pragma unroll 1
+    for (int j = 0; j < 32; ++j) {
+        const float d = __shfl_sync(0xffffffffu, a[0], j);
+        const bool ok = d > 0.f;
+        const float rs = ok ? rsqrtf(d) : 0.f;
+        failed |= (ok || j >= kq) ? 0u : (1u << j);
+        const float l = (lane == j) ? (ok ? d * rs : d) : (lane > j ? a[0] * rs : 0.f);
+        if (lane >= j) sLs[j * 32 + (lane - j)] = l;
+        if (lane == 0) sRs[j] = rs;
+        __syncwarp();
+        const float4 *c4 = reinterpret_cast<const float4 *>(sLs + j * 32);
+#pragma unroll
+        for (int m4 = 0; m4 < 8; ++m4) {
+            const float4 v4 = c4[m4];
+            const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = 4 * m4 + e;
+                if (m == 0) continue;
+                a[m - 1] = fmaf(-l, cv[e], a[m]);          // column j+m -= L(lane, j) * L(j+m, j)
+            }
+        }
+        a[31] = 0.f;
+    }
+    return failed;
+}
+
+// Solve the rows below the diagonal block against it (L21 = A21 * L11^-T), one column per step
+// in a compact loop with the same shifting frame: x_k = v[0] / L(k,k), then the later columns
+// v[m-1] = v[m] - x_k * L(k+m, k). Each x_k goes to global memory (row g, column Q0 + k) and,
+// when `panel` is set, split into the operand panel row p. TWO: a second row (vb) per thread.
+template <bool UPPER, bool TWO>
+__device__ __forceinline__ void solve_rows(float (&va)[32], float (&vb)[32], bool stA, bool stB, bool panel,
+                                           float *A, int64_t lda, int gA, int gB, int pA, int pB, int Q0, int kq,
+                                           const float *sLs, const float *sRs, unsigned char *p_hi,
+                                           unsigned char *p_lo) {
+#pragma unroll 1
+    for (int k = 0; k < 32; ++k) {
+        const float r = sRs[k];
+        const bool kin = k < kq;
+        const float xa = kin ? va[0] * r : 0.f;
+        const float xb = (TWO && kin) ? vb[0] * r : 0.f;
+        if (kin) {
+            if (stA) A[sidx<UPPER>(gA, Q0 + k, lda)] = xa;
+            if (TWO && stB) A[sidx<UPPER>(gB, Q0 + k, lda)] = xb;
+        }
+        if (panel) {
+            if (stA) panel_elem(p_hi, p_lo, pA, k, xa);
+            if (TWO && stB) panel_elem(p_hi, p_lo, pB, k, xb);
+        }
+        const float4 *l4p = reinterpret_cast<const float4 *>(sLs + k * 32);
+#pragma unroll
+        for (int m4 = 0; m4 < 8; ++m4) {
+            const float4 l4 = l4p[m4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = 4 * m4 + e;
+                if (m == 0) continue;
+                va[m - 1] = fmaf(-xa, lv[e], va[m]);
+                if (TWO) vb[m - 1] = fmaf(-xb, lv[e], vb[m]);
+            }
+        }
+        va[31] = 0.f;
+        if (TWO) vb[31] = 0.f;
+    }
+}
+
+}  // namespace colblk
+
+template <typename T, bool UPPER>
+__global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) {
+    static_assert(sizeof(T) == 4 && !is_cplx<T>::value, "column-block tensor-core kernel: f32");
+    using C = ColBlkCfg;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char *p_hi = sm + C::P0_HI;
+    unsigned char *p_lo = sm + C::P0_LO;
+    float *sLs = reinterpret_cast<float *>(sm + C::OFF_L11);
+    float *sRs = reinterpret_cast<float *>(sm + C::OFF_RS);
+    __shared__ uint32_t s_tmem;
+    __shared__ uint64_t s_mbar[2];                 // MMA completion, per operand panel
+    __shared__ int s_stop;     // 0 running, 2 a bounded wait gave up
+    __shared__ int s_diag;     // failing column of the current diagonal block, -1 none
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t mat = blockIdx.x;
+    const int n = args.n;
+    float *A = static_cast<T *>(args.A) + mat * args.stride_a;
+    const int64_t lda = args.lda;
+    if (args.mode != MODE_POTRF) return;      // factor-only variant (the dispatcher never asks otherwise)
+
+    if (warp == 0) {
+        tc::tmem_alloc(&s_tmem, 512);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        tc::mbar_init(&s_mbar[0], 1);
+        tc::mbar_init(&s_mbar[1], 1);
+        tc::mbar_fence_init();
+        s_stop = 0;
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+    const uint32_t s_base = tc::smem_u32(sm);
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;   // this warp's tensor-memory lanes
+    constexpr uint32_t kPolls = 1u << 24;
+    uint32_t phase = 0;                      // bit b: parity to wait for on panel b's mbarrier
+    uint32_t pend = 0;                       // bit b: a committed batch reading panel b not yet waited for
+    int lost = -1;                           // panel whose wait gave up here (its batch may still run)
+    // wait for the last committed batch that reads panel b (every thread polls the mbarrier;
+    // bounded). A wait that gives up flags the item; no further MMAs are issued after the next
+    // barrier.
+    auto wait_mma = [&](int b) {
+        if (pend & (1u << b)) {
+            if (tc::mbar_wait(&s_mbar[b], (phase >> b) & 1u, kPolls)) phase ^= 1u << b;
+            else { s_stop = 2; lost = b; }
+            pend &= ~(1u << b);
+        }
+        tc::fence_after_sync();
+    };
+
+    // rows of the block column owned by this thread (block-relative) and their row tiles; the
+    // tile's tensor-memory lanes 32*(warp&3).. are the ones this warp may read
+    const int rA = tid, rB = tid + 256;
+    const int tA = warp >> 2, tB = 2 + (warp >> 2);
+    bool stop = false;
+
+    for (int C0 = 0; C0 < n && !stop; C0 += C::W) {
+        const int M = n - C0;
+        const int Wb = M < C::W ? M : C::W;
+        const int mtiles = (M + 127) >> 7;
+        const int Nb = (Wb + 15) & ~15;      // MMA N: a multiple of 16 (columns past Wb are unused)
+
+        // ---------------------------------------------- 1. block update from the finished columns
+        const int nk = C0 >> 5;
+        if (nk > 0) {
+            float xa[32], xb[32];
+            colblk::load_row<UPPER>(A, lda, C0 + rA, 0, rA < M ? 32 : 0, xa);
+            colblk::load_row<UPPER>(A, lda, C0 + rB, 0, rB < M ? 32 : 0, xb);
+            // double-buffered: chunk kc goes to panel kc&1 while the MMAs of chunk kc-1 run
+            for (int kc = 0; kc < nk; ++kc) {
+                const int pb = kc & 1;
+                wait_mma(pb);                                // chunk kc-2's MMAs are done: panel pb is free
+                unsigned char *bh = sm + (pb ? C::P1_HI : C::P0_HI), *bl = sm + (pb ? C::P1_LO : C::P0_LO);
+                if (rA < M) colblk::panel_row(bh, bl, rA, xa);
+                if (rB < M) colblk::panel_row(bh, bl, rB, xb);
+                tc::fence_proxy_async_smem();
+                tc::fence_before_sync();
+                __syncthreads();
+                tc::fence_after_sync();
+                if (s_stop) { stop = true; break; }          // uniform: read after the barrier
+                if (tid == 0) {
+                    for (int t = 0; t < mtiles; ++t)
+                        colblk::mma_chunk(tmem + static_cast<uint32_t>(t * 128),
+                                          s_base + static_cast<uint32_t>(pb ? C::P1_HI : C::P0_HI),
+                                          s_base + static_cast<uint32_t>(pb ? C::P1_LO : C::P0_LO), 128 * t, 0, Nb, kc > 0);
+                    tc::mma_commit(&s_mbar[pb]);
+                }
+                pend |= 1u << pb;
+                if (kc + 1 < nk) {                           // next chunk's loads overlap these MMAs
+                    colblk::load_row<UPPER>(A, lda, C0 + rA, 32 * (kc + 1), rA < M ? 32 * (kc + 2) : 0, xa);
+                    colblk::load_row<UPPER>(A, lda, C0 + rB, 32 * (kc + 1), rB < M ? 32 * (kc + 2) : 0, xb);
+                }
+            }
+        }
+
+        // ---------------------------------------------- 2. factor the block column, 32 columns at a time
+        for (int q = 0; 32 * q < Wb && !stop; ++q) {
+            const int Q0 = C0 + 32 * q;
+            const int kq = min(32, n - Q0);
+            const int rlo = 32 * q;                          // the slice's diagonal rows start here
+            const bool liveA = rA >= rlo && rA < M, liveB = rB < M;
+            float va[32], vb[32];
+            colblk::load_row<UPPER>(A, lda, C0 + rA, Q0, liveA ? Q0 + kq : 0, va);
+            colblk::load_row<UPPER>(A, lda, C0 + rB, Q0, liveB ? Q0 + kq : 0, vb);
+            wait_mma(0);
+            wait_mma(1);
+            if (C0 > 0 || q > 0) {                           // the accumulator holds this slice's update
+                if (tA < mtiles && (warp >= 4 || warp >= q)) {
+                    float d[32];
+                    tc::tmem_ld32(tmem + lane_base + static_cast<uint32_t>(tA * 128 + 32 * q), d);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) va[c] -= d[c];
+                }
+                if (tB < mtiles) {
+                    float d[32];
+                    tc::tmem_ld32(tmem + lane_base + static_cast<uint32_t>(tB * 128 + 32 * q), d);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) vb[c] -= d[c];
+                }
+            }
+            // diagonal block: warp q holds its rows (lane l = row Q0 + l); padding rows are identity
+            if (warp == q) {
+                float a[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) a[c] = (lane < kq) ? (c <= lane ? va[c] : 0.f) : (c == lane ? 1.f : 0.f);
+                const unsigned failed = colblk::factor_diag(a, lane, kq, sLs, sRs);
+                __syncwarp();
+                // the diagonal block's lower part (columns before a failure are final)
+                if (lane < kq) {
+#pragma unroll 1
+                    for (int c = 0; c <= lane; ++c) A[colblk::sidx<UPPER>(Q0 + lane, Q0 + c, lda)] = sLs[c * 32 + lane - c];
+                }
+                if (lane == 0) s_diag = failed ? __ffs(failed) - 1 : -1;
+            }
+            __syncthreads();
+            if (s_stop || s_diag >= 0) {                     // uniform: read after the barrier
+                if (tid == 0 && !s_stop) args.info[mat] = Q0 + s_diag + 1;
+                stop = true;
+                break;
+            }
+            // rows below the diagonal block: L21 = A21 * L11^-T, one row per thread and tile
+            const bool next = 32 * (q + 1) < Wb;             // the block has further slices
+            const bool solA = rA >= rlo + 32 && rA < M;
+            if (tB < mtiles)                                 // warp-uniform: this warp has a second row tile
+                colblk::solve_rows<UPPER, true>(va, vb, solA, liveB, next, A, lda, C0 + rA, C0 + rB, rA, rB, Q0, kq,
+                                                sLs, sRs, p_hi, p_lo);
+            else if (solA)
+                colblk::solve_rows<UPPER, false>(va, vb, solA, false, next, A, lda, C0 + rA, C0 + rB, rA, rB, Q0, kq,
+                                                 sLs, sRs, p_hi, p_lo);
+            if (next) {
+                // D[:, 32(q+1) : Nb) += L21 * L21^T over this slice: A = every row tile of the
+                // panel, B = the panel rows of the block's remaining columns
+                tc::fence_proxy_async_smem();
+                tc::fence_before_sync();
+                __syncthreads();
+                tc::fence_after_sync();
+                if (tid == 0) {
+                    const int c1 = 32 * (q + 1);
+                    for (int t = 0; t < mtiles; ++t)
+                        colblk::mma_chunk(tmem + static_cast<uint32_t>(t * 128 + c1),
+                                          s_base + static_cast<uint32_t>(C::P0_HI), s_base + static_cast<uint32_t>(C::P0_LO),
+                                          128 * t, c1, Nb - c1, C0 > 0 || q > 0);
+                    tc::mma_commit(&s_mbar[0]);
+                }
+                pend |= 1u;
+            } else {
+                tc::fence_before_sync();
+                __syncthreads();                             // L11 and the panel are free again
+                tc::fence_after_sync();
+            }
+        }
+    }
+    wait_mma(0);
+    wait_mma(1);
+    if (lost >= 0) tc::mbar_wait(&s_mbar[lost], (phase >> lost) & 1u, kPolls);  // once more for the batch given up on
+    __syncthreads();
+    if (tid == 0) {
+        if (s_stop == 2) args.info[mat] = -1;
+        else if (!stop) args.info[mat] = 0;
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+}  // namespace bl

@@ -78,7 +78,7 @@ std::string spelling(const KernelEntry &e) {
     else if (e.family == 2)   // nb bit 0: whole squares, bit 1: packed f32x2 update
         snprintf(buf, sizeof buf, "warp:p=%d:r=%d%s%s", e.p, e.s, (e.nb & 1) ? ":full=1" : "", (e.nb & 2) ? ":x2=1" : "");
     else if (e.family == 3) snprintf(buf, sizeof buf, "thread:n=%d", e.nb);
-    else if (e.s) snprintf(buf, sizeof buf, "blocked:nb=%d:tc=1", e.nb);   // tensor-core trailing update
+    else if (e.s) snprintf(buf, sizeof buf, "blocked:nb=%d:tc=%d", e.nb, e.s);   // tensor-core update (1: trailing, 2: column block)
     else snprintf(buf, sizeof buf, "blocked:nb=%d", e.nb);
     return buf;
 }

@@ -42,6 +42,7 @@ static const KernelEntry k_entries_f32[] = {
     blocked_entry<float, 32>(),
     blocked_entry<float, 64>(),
     blocked_entry<float, 32, true>(),
+    colblock_entry<float>(),
 };
 
 const KernelEntry *entries_f32(int *count) {

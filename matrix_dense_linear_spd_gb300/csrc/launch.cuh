@@ -8,6 +8,7 @@
 #include "bl_types.cuh"
 #include "registry.h"
 #include "blocked_kernel.cuh"
+#include "colblock_kernel.cuh"
 #include "tile_kernel.cuh"
 #include "warp_kernel.cuh"
 #include "thread_kernel.cuh"
@@ -142,6 +143,28 @@ template <typename T, int P, int S>
 constexpr KernelEntry tile_entry() {
     using C = TileCfg<T, P, S>;
     return KernelEntry{0, P, S, 0, C::N, P, C::THREADS, C::G, C::smem_bytes, &launch_tile<T, P, S>};
+}
+
+template <typename T>
+cudaError_t launch_colblock(const BatchArgs &a, cudaStream_t st) {
+    static std::atomic<unsigned long long> done{0};
+    static std::atomic<unsigned long long> done_u{0};
+    cudaError_t e = a.upper ? ensure_smem(colblock_kernel<T, true>, ColBlkCfg::smem_bytes, done_u)
+                            : ensure_smem(colblock_kernel<T, false>, ColBlkCfg::smem_bytes, done);
+    if (e != cudaSuccess) return e;
+    if (a.upper)
+        colblock_kernel<T, true><<<static_cast<unsigned>(a.batch), ColBlkCfg::THREADS, ColBlkCfg::smem_bytes, st>>>(a);
+    else
+        colblock_kernel<T, false><<<static_cast<unsigned>(a.batch), ColBlkCfg::THREADS, ColBlkCfg::smem_bytes, st>>>(a);
+    return cudaGetLastError();
+}
+
+// The column-block tensor-core kernel (f32 potrf, n <= 512): blocked family, panel width 32,
+// spelled with tc=2; factor only.
+template <typename T>
+constexpr KernelEntry colblock_entry() {
+    return KernelEntry{1, 0, 2, 32, ColBlkCfg::MAXN, -1, ColBlkCfg::THREADS, 1, ColBlkCfg::smem_bytes,
+                       &launch_colblock<T>};
 }
 
 template <typename T, int NB, bool TC = false>
