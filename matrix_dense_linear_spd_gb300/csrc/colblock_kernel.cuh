@@ -8,17 +8,21 @@
 //   1. block update on the tensor cores, left-looking: D = L(C0:n, 0:C0) * L(C0:C0+W, 0:C0)^T,
 //      K in chunks of 32 columns of L. Each chunk is read once from global memory, split into
 //      tf32 hi and lo parts (3xTF32: hi*hi + hi*lo + lo*hi keeps f32 accuracy) and stored as a
-//      128-byte-swizzled K-major operand panel; the B operand is the panel's first W rows.
-//      D lives in tensor memory, one 128 x W tile per 128 rows (4 tiles = all 512 columns).
+//      128-byte-swizzled K-major operand panel (two panels, alternating, so a chunk is staged
+//      while the previous one multiplies); the B operand is the panel's first W rows. D lives in
+//      tensor memory, one 128 x W tile per 128 rows (4 tiles = all 512 columns).
 //   2. the block column is factored right-looking, 32 columns (one slice) at a time. The slice's
-//      current values are S(:, slice) - D(:, slice): original values from global memory minus
-//      the accumulator read back with tcgen05.ld. One warp factors the 32 x 32 diagonal block in
-//      registers (pivot and column entries by shuffles; first non-positive pivot fails the item);
-//      every thread then solves its rows against it (L21 = A21 * L11^-T) and writes them to
-//      global memory. When the block has further slices, the solved rows are split into the
-//      operand panel and the tensor cores add L21 * L21^T to D for the block's remaining columns.
+//      current values V = S(:, slice) - D(:, slice) are the original values from global memory
+//      minus the accumulator read back with tcgen05.ld. One warp factors the 32 x 32 diagonal
+//      block (first non-positive pivot fails the item) and inverts it; meanwhile the other rows
+//      go, split, into the operand panel. The panel solve L21 = V * L11^-T then runs on the
+//      tensor cores as V * Linv^T into the slice's own accumulator columns; the rows are read
+//      back, written to global memory and, when the block has further slices, split into the
+//      panel again, from where the tensor cores add L21 * L21^T to D for the block's remaining
+//      columns.
 // Each element of the referenced triangle is read from global memory once as input and written
-// once; later blocks read finished L columns (from L2) as operands.
+// once; later blocks read finished L columns (from L2) as operands. Using L11^-1 for the panel
+// solve adds a relative error of order cond(L11) * eps (cond(L11) <= sqrt(cond(A))).
 //
 // Upper runs on the view S(i,k) = A(k,i) (real type: no conjugation); only the referenced
 // triangle is ever written. A failure at column c reports info = c + 1 and the item stops (the
@@ -45,9 +49,11 @@ struct ColBlkCfg {
     static constexpr size_t P1_LO = P1_HI + static_cast<size_t>(MAXN - W) * 128;
     static constexpr size_t OFF_L11 = P1_HI;                        // sLs[c*32 + m] = L(c+m, c)
     static constexpr size_t OFF_RS = OFF_L11 + 32 * 32 * 4;         // 1 / L(c, c)
+    static constexpr size_t OFF_BI_HI = P1_HI + 8192;               // Linv, 32 rows x 128 bytes, hi
+    static constexpr size_t OFF_BI_LO = OFF_BI_HI + 4096;           // and lo
     static constexpr size_t END = P1_LO + static_cast<size_t>(MAXN - W) * 128;
     static constexpr size_t smem_bytes = 1024 + END;                // + 1024 for the panel alignment
-    static_assert(OFF_RS + 32 * 4 <= END, "diagonal-block area inside panel 1");
+    static_assert(OFF_RS + 32 * 4 <= OFF_BI_HI && OFF_BI_LO + 4096 <= END, "diagonal-block area inside panel 1");
 };
 
 namespace colblk {
@@ -90,99 +96,122 @@ __device__ __forceinline__ void panel_elem(unsigned char *hi, unsigned char *lo,
     *reinterpret_cast<float *>(lo + off) = l;
 }
 
-// D[:, 0:N) (+)= A * B^T over K = 32 with the 3xTF32 split: A = panel rows [a_row0, a_row0 + 128),
-// B = panel rows [b_row0, b_row0 + N). `acc` false overwrites D on the first product.
-__device__ __forceinline__ void mma_chunk(uint32_t d, uint32_t s_hi, uint32_t s_lo, int a_row0, int b_row0, int N,
-                                          bool acc) {
+// D[:, 0:N) (+)= A * B^T over K = 32 with the 3xTF32 split (hi*hi + hi*lo + lo*hi): A is 128 rows
+// at a_hi / a_lo, B is N rows at b_hi / b_lo (shared-memory addresses of 128-byte-swizzled
+// K-major tiles). `acc` false overwrites D on the first product.
+__device__ __forceinline__ void mma_k32(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo, int N,
+                                        bool acc) {
     const uint32_t idesc = tc::idesc_tf32(128, N);
-    const uint32_t ah = s_hi + static_cast<uint32_t>(a_row0) * 128u, al = s_lo + static_cast<uint32_t>(a_row0) * 128u;
-    const uint32_t bh = s_hi + static_cast<uint32_t>(b_row0) * 128u, bl_ = s_lo + static_cast<uint32_t>(b_row0) * 128u;
 #pragma unroll
     for (int st = 0; st < 4; ++st) {
-        tc::mma_tf32(d, tc::sdesc_sw128(ah + 32 * st), tc::sdesc_sw128(bh + 32 * st), idesc, acc || st > 0);
-        tc::mma_tf32(d, tc::sdesc_sw128(ah + 32 * st), tc::sdesc_sw128(bl_ + 32 * st), idesc, true);
-        tc::mma_tf32(d, tc::sdesc_sw128(al + 32 * st), tc::sdesc_sw128(bh + 32 * st), idesc, true);
+        tc::mma_tf32(d, tc::sdesc_sw128(a_hi + 32 * st), tc::sdesc_sw128(b_hi + 32 * st), idesc, acc || st > 0);
+        tc::mma_tf32(d, tc::sdesc_sw128(a_hi + 32 * st), tc::sdesc_sw128(b_lo + 32 * st), idesc, true);
+        tc::mma_tf32(d, tc::sdesc_sw128(a_lo + 32 * st), tc::sdesc_sw128(b_hi + 32 * st), idesc, true);
     }
+}
+
+// One step of the diagonal-block factor in a shifting frame of F live columns: a[0] is the
+// current column j, a[m] column j+m. Publishes L(j+m, j) to sLs[j*32 + m] and 1/L(j,j) to
+// sRs[j]; the next column takes L(j+1, j) by a shuffle, and the next pivot itself,
+// A(j+1,j+1) - L(j+1,j)^2, is formed by its own lane and broadcast into d; the rest of the update
+// reads the published column back as 16-byte broadcasts (positions past the block hold stale
+// values and only touch entries past the block). (Each further shuffle on this chain measured
+// slower than the shared-memory path it replaces.)
+template <int F>
+__device__ __forceinline__ void factor_step(float (&a)[32], int lane, int j, int kq, float &d, unsigned &failed,
+                                            float *sLs, float *sRs) {
+    const bool ok = d > 0.f;
+    const float rs = ok ? rsqrtf(d) : 0.f;
+    failed |= (ok || j >= kq) ? 0u : (1u << j);
+    const float l = (lane == j) ? (ok ? d * rs : d) : (lane > j ? a[0] * rs : 0.f);
+    if (lane >= j) sLs[j * 32 + (lane - j)] = l;
+    if (lane == 0) sRs[j] = rs;
+    d = __shfl_sync(0xffffffffu, fmaf(-l, l, a[1]), (j + 1) & 31);   // lane j+1: its next pivot
+    const float l1 = __shfl_sync(0xffffffffu, l, (j + 1) & 31);
+    const float a0 = fmaf(-l, l1, a[1]);
+    __syncwarp();
+    const float4 *c4 = reinterpret_cast<const float4 *>(sLs + j * 32);
+#pragma unroll
+    for (int m4 = 0; m4 < (F + 3) / 4; ++m4) {
+        const float4 v4 = c4[m4];
+        const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int m = 4 * m4 + e;
+            if (m < 2 || m >= F) continue;
+            a[m - 1] = fmaf(-l, cv[e], a[m]);              // column j+m -= L(lane, j) * L(j+m, j)
+        }
+    }
+    a[0] = a0;
+    a[F - 1] = 0.f;
+}
+
+// One step of the inverse (column `lane` of Linv, shifting frame of F live rows): acc[0] is row
+// k of the running right-hand side; Linv(k, lane) = acc[0] / L(k,k) goes, split, to row k of the
+// operand tile; the later rows subtract L(k+m, k) * Linv(k, lane).
+template <int F>
+__device__ __forceinline__ void invert_step(float (&acc)[32], int lane, int k, const float *sLs, const float *sRs,
+                                            unsigned char *b_hi, unsigned char *b_lo) {
+    const float y = acc[0] * sRs[k];
+    const float4 *c4 = reinterpret_cast<const float4 *>(sLs + k * 32);
+#pragma unroll
+    for (int m4 = 0; m4 < (F + 3) / 4; ++m4) {
+        const float4 v4 = c4[m4];
+        const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int m = 4 * m4 + e;
+            if (m == 0 || m >= F) continue;
+            acc[m - 1] = fmaf(-y, cv[e], acc[m]);
+        }
+    }
+    acc[F - 1] = 0.f;
+    panel_elem(b_hi, b_lo, k, lane, y);
 }
 
 // Factor the 32 x 32 diagonal block held by one warp (lane = row; padding rows are identity),
-// right-looking, one column per step in a compact loop: the lane's row is kept in a shifting
-// frame (a[0] is always the current column), so every register index is static and the loop
-// body stays small enough for the instruction cache. Column j of L is published to sLs[j*32 + m]
-// = L(j+m, j) (m = 0 is the diagonal), 1/L(j,j) to sRs[j]; the update reads the column back as
-// 16-byte broadcasts (positions past the block hold stale values and only touch entries past
-// the block). Returns the failure bit mask.
+// right-looking, one column per step in a compact loop over the full-width frame. (A frame that
+// narrows with the finished columns measured slower here: the chain is latency-bound, and the
+// extra loop boundaries cost more than the FMAs they save.) Returns the failure bit mask.
 __device__ __forceinline__ unsigned factor_diag(float (&a)[32], int lane, int kq, float *sLs, float *sRs) {
     unsigned failed = 0;
+    float d = __shfl_sync(0xffffffffu, a[0], 0);
 #pragma unroll 1
-    for (int j = 0; j < 32; ++j) {
-        const float d = __shfl_sync(0xffffffffu, a[0], j);
-        const bool ok = d > 0.f;
-        const float rs = ok ? rsqrtf(d) : 0.f;
-        failed |= (ok || j >= kq) ? 0u : (1u << j);
-        const float l = (lane == j) ? (ok ? d * rs : d) : (lane > j ? a[0] * rs : 0.f);
-        if (lane >= j) sLs[j * 32 + (lane - j)] = l;
-        if (lane == 0) sRs[j] = rs;
-        __syncwarp();
-        const float4 *c4 = reinterpret_cast<const float4 *>(sLs + j * 32);
-#pragma unroll
-        for (int m4 = 0; m4 < 8; ++m4) {
-            const float4 v4 = c4[m4];
-            const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = 4 * m4 + e;
-                if (m == 0) continue;
-                a[m - 1] = fmaf(-l, cv[e], a[m]);          // column j+m -= L(lane, j) * L(j+m, j)
-            }
-        }
-        a[31] = 0.f;
-    }
+    for (int j = 0; j < 32; ++j) factor_step<32>(a, lane, j, kq, d, failed, sLs, sRs);
     return failed;
 }
 
-// Solve the rows below the diagonal block against it (L21 = A21 * L11^-T), one column per step
-// in a compact loop with the same shifting frame: x_k = v[0] / L(k,k), then the later columns
-// v[m-1] = v[m] - x_k * L(k+m, k). Each x_k goes to global memory (row g, column Q0 + k) and,
-// when `panel` is set, split into the operand panel row p. TWO: a second row (vb) per thread.
-template <bool UPPER, bool TWO>
-__device__ __forceinline__ void solve_rows(float (&va)[32], float (&vb)[32], bool stA, bool stB, bool panel,
-                                           float *A, int64_t lda, int gA, int gB, int pA, int pB, int Q0, int kq,
-                                           const float *sLs, const float *sRs, unsigned char *p_hi,
-                                           unsigned char *p_lo) {
+// Inverse of the factored diagonal block, Linv = L11^-1 (lower triangular), by one warp: lane c
+// forward-substitutes the unit vector e_c with the columns of L11 from sLs / sRs (in a shifting
+// frame like the factor's), producing column c of Linv; Linv(k, c) is stored split into tf32 hi and lo at row k, K
+// index c of a 32-row operand tile, so the tile holds Linv row by row (the B operand of
+// X = V * Linv^T). The frame narrows by 8 every 8 steps (32, 24, 16, 8 live rows), so no work is
+// spent on rows already finished.
+__device__ __forceinline__ void invert_diag(int lane, const float *sLs, const float *sRs, unsigned char *b_hi,
+                                            unsigned char *b_lo) {
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = (i == lane) ? 1.f : 0.f;
 #pragma unroll 1
-    for (int k = 0; k < 32; ++k) {
-        const float r = sRs[k];
-        const bool kin = k < kq;
-        const float xa = kin ? va[0] * r : 0.f;
-        const float xb = (TWO && kin) ? vb[0] * r : 0.f;
-        if (kin) {
-            if (stA) A[sidx<UPPER>(gA, Q0 + k, lda)] = xa;
-            if (TWO && stB) A[sidx<UPPER>(gB, Q0 + k, lda)] = xb;
-        }
-        if (panel) {
-            if (stA) panel_elem(p_hi, p_lo, pA, k, xa);
-            if (TWO && stB) panel_elem(p_hi, p_lo, pB, k, xb);
-        }
-        const float4 *l4p = reinterpret_cast<const float4 *>(sLs + k * 32);
+    for (int k = 0; k < 8; ++k) invert_step<32>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+#pragma unroll 1
+    for (int k = 8; k < 16; ++k) invert_step<24>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+#pragma unroll 1
+    for (int k = 16; k < 24; ++k) invert_step<16>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+#pragma unroll 1
+    for (int k = 24; k < 32; ++k) invert_step<8>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+}
+
+// S(i, k0 + c) = v[c] for c < cend.
+template <bool UPPER>
+__device__ __forceinline__ void store_row(float *A, int64_t lda, int i, int k0, int cend, const float (&v)[32]) {
 #pragma unroll
-        for (int m4 = 0; m4 < 8; ++m4) {
-            const float4 l4 = l4p[m4];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = 4 * m4 + e;
-                if (m == 0) continue;
-                va[m - 1] = fmaf(-xa, lv[e], va[m]);
-                if (TWO) vb[m - 1] = fmaf(-xb, lv[e], vb[m]);
-            }
-        }
-        va[31] = 0.f;
-        if (TWO) vb[31] = 0.f;
-    }
+    for (int c = 0; c < 32; ++c)
+        if (c < cend) A[sidx<UPPER>(i, k0 + c, lda)] = v[c];
 }
 
 }  // namespace colblk
+
 
 template <typename T, bool UPPER>
 __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) {
@@ -269,10 +298,11 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
                 tc::fence_after_sync();
                 if (s_stop) { stop = true; break; }          // uniform: read after the barrier
                 if (tid == 0) {
-                    for (int t = 0; t < mtiles; ++t)
-                        colblk::mma_chunk(tmem + static_cast<uint32_t>(t * 128),
-                                          s_base + static_cast<uint32_t>(pb ? C::P1_HI : C::P0_HI),
-                                          s_base + static_cast<uint32_t>(pb ? C::P1_LO : C::P0_LO), 128 * t, 0, Nb, kc > 0);
+                    const uint32_t ph = s_base + static_cast<uint32_t>(pb ? C::P1_HI : C::P0_HI);
+                    const uint32_t pl = s_base + static_cast<uint32_t>(pb ? C::P1_LO : C::P0_LO);
+                    for (int t = 0; t < mtiles; ++t)     // B: the block's own rows, the panel's first Nb
+                        colblk::mma_k32(tmem + static_cast<uint32_t>(t * 128), ph + 16384u * t, pl + 16384u * t, ph, pl,
+                                        Nb, kc > 0);
                     tc::mma_commit(&s_mbar[pb]);
                 }
                 pend |= 1u << pb;
@@ -308,8 +338,18 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
                     for (int c = 0; c < 32; ++c) vb[c] -= d[c];
                 }
             }
-            // diagonal block: warp q holds its rows (lane l = row Q0 + l); padding rows are identity
+            if (kq < 32) {                                   // ragged last slice: no values past n
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    if (c >= kq) va[c] = 0.f;
+                    if (c >= kq) vb[c] = 0.f;
+                }
+            }
+            const bool solA = rA >= rlo + 32 && rA < M;     // rows below the diagonal block
+            // diagonal block: warp q holds its rows (lane l = row Q0 + l); padding rows are identity.
+            // It factors them, stores them, and inverts L11 into the B tile of the solve.
             if (warp == q) {
+                if (liveB) colblk::panel_row(p_hi, p_lo, rB, vb);   // this warp's lower rows first
                 float a[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) a[c] = (lane < kq) ? (c <= lane ? va[c] : 0.f) : (c == lane ? 1.f : 0.f);
@@ -320,23 +360,43 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
 #pragma unroll 1
                     for (int c = 0; c <= lane; ++c) A[colblk::sidx<UPPER>(Q0 + lane, Q0 + c, lda)] = sLs[c * 32 + lane - c];
                 }
+                colblk::invert_diag(lane, sLs, sRs, sm + C::OFF_BI_HI, sm + C::OFF_BI_LO);
                 if (lane == 0) s_diag = failed ? __ffs(failed) - 1 : -1;
             }
+            // meanwhile the rows below go, split, into the panel: the A operand of the solve
+            if (solA) colblk::panel_row(p_hi, p_lo, rA, va);
+            if (liveB && warp != q) colblk::panel_row(p_hi, p_lo, rB, vb);
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
             __syncthreads();
+            tc::fence_after_sync();
             if (s_stop || s_diag >= 0) {                     // uniform: read after the barrier
                 if (tid == 0 && !s_stop) args.info[mat] = Q0 + s_diag + 1;
                 stop = true;
                 break;
             }
-            // rows below the diagonal block: L21 = A21 * L11^-T, one row per thread and tile
+            // L21 = A21 * L11^-T = V * Linv^T on the tensor cores, into this slice's accumulator
+            // columns (their update was consumed above)
+            if (tid == 0) {
+                for (int t = 0; t < mtiles; ++t)
+                    colblk::mma_k32(tmem + static_cast<uint32_t>(t * 128 + 32 * q), s_base + static_cast<uint32_t>(C::P0_HI) + 16384u * t,
+                                    s_base + static_cast<uint32_t>(C::P0_LO) + 16384u * t,
+                                    s_base + static_cast<uint32_t>(C::OFF_BI_HI), s_base + static_cast<uint32_t>(C::OFF_BI_LO),
+                                    32, false);
+                tc::mma_commit(&s_mbar[0]);
+            }
+            pend |= 1u;
+            wait_mma(0);
             const bool next = 32 * (q + 1) < Wb;             // the block has further slices
-            const bool solA = rA >= rlo + 32 && rA < M;
-            if (tB < mtiles)                                 // warp-uniform: this warp has a second row tile
-                colblk::solve_rows<UPPER, true>(va, vb, solA, liveB, next, A, lda, C0 + rA, C0 + rB, rA, rB, Q0, kq,
-                                                sLs, sRs, p_hi, p_lo);
-            else if (solA)
-                colblk::solve_rows<UPPER, false>(va, vb, solA, false, next, A, lda, C0 + rA, C0 + rB, rA, rB, Q0, kq,
-                                                 sLs, sRs, p_hi, p_lo);
+            const bool xA = tA < mtiles && (warp >= 4 || warp > q), xB = tB < mtiles;   // warp-uniform
+            if (xA) tc::tmem_ld32(tmem + lane_base + static_cast<uint32_t>(tA * 128 + 32 * q), va);
+            if (xB) tc::tmem_ld32(tmem + lane_base + static_cast<uint32_t>(tB * 128 + 32 * q), vb);
+            if (solA) colblk::store_row<UPPER>(A, lda, C0 + rA, Q0, kq, va);
+            if (liveB) colblk::store_row<UPPER>(A, lda, C0 + rB, Q0, kq, vb);
+            if (next) {
+                if (solA) colblk::panel_row(p_hi, p_lo, rA, va);
+                if (liveB) colblk::panel_row(p_hi, p_lo, rB, vb);
+            }
             if (next) {
                 // D[:, 32(q+1) : Nb) += L21 * L21^T over this slice: A = every row tile of the
                 // panel, B = the panel rows of the block's remaining columns
@@ -346,10 +406,10 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
                 tc::fence_after_sync();
                 if (tid == 0) {
                     const int c1 = 32 * (q + 1);
+                    const uint32_t ph = s_base + static_cast<uint32_t>(C::P0_HI), pl = s_base + static_cast<uint32_t>(C::P0_LO);
                     for (int t = 0; t < mtiles; ++t)
-                        colblk::mma_chunk(tmem + static_cast<uint32_t>(t * 128 + c1),
-                                          s_base + static_cast<uint32_t>(C::P0_HI), s_base + static_cast<uint32_t>(C::P0_LO),
-                                          128 * t, c1, Nb - c1, C0 > 0 || q > 0);
+                        colblk::mma_k32(tmem + static_cast<uint32_t>(t * 128 + c1), ph + 16384u * t, pl + 16384u * t,
+                                        ph + 128u * c1, pl + 128u * c1, Nb - c1, C0 > 0 || q > 0);
                     tc::mma_commit(&s_mbar[0]);
                 }
                 pend |= 1u;
