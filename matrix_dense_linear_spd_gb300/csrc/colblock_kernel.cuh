@@ -6,11 +6,12 @@
 // contraction). The columns are taken in blocks of W = 128; for the block C0 .. C0+W-1, whose
 // lower part has M = n - C0 rows:
 //   1. block update on the tensor cores, left-looking: D = L(C0:n, 0:C0) * L(C0:C0+W, 0:C0)^T,
-//      K in chunks of 32 columns of L. Each chunk is read once from global memory, split into
-//      tf32 hi and lo parts (3xTF32: hi*hi + hi*lo + lo*hi keeps f32 accuracy) and stored as a
-//      128-byte-swizzled K-major operand panel (two panels, alternating, so a chunk is staged
-//      while the previous one multiplies); the B operand is the panel's first W rows. D lives in
-//      tensor memory, one 128 x W tile per 128 rows (4 tiles = all 512 columns).
+//      K in chunks of 32 columns of L. Each chunk is read once from global memory (two chunks
+//      ahead, into registers), split into tf32 hi and lo parts (3xTF32: hi*hi + hi*lo + lo*hi
+//      keeps f32 accuracy) and stored as a 128-byte-swizzled K-major operand panel (two panels,
+//      alternating, so a chunk is staged while the previous one multiplies); the B operand is
+//      the panel's first W rows. D lives in tensor memory, one 128 x W tile per 128 rows (4 tiles
+//      = all 512 columns).
 //   2. the block column is factored right-looking, 32 columns (one slice) at a time. The slice's
 //      current values V = S(:, slice) - D(:, slice) are the original values from global memory
 //      minus the accumulator read back with tcgen05.ld. One warp factors the 32 x 32 diagonal
@@ -64,9 +65,24 @@ __device__ __forceinline__ int64_t sidx(int i, int k, int64_t lda) {
     return UPPER ? static_cast<int64_t>(i) * lda + k : static_cast<int64_t>(k) * lda + i;
 }
 
-// S(i, k0 + c) for c < 32 into v; entries with k0 + c >= kend are 0 (kend <= k0: all 0).
+// S(i, k0 + c) for c < 32 into v; entries with k0 + c >= kend are 0 (kend <= k0: all 0). Upper
+// rows of S are contiguous in memory: with `vec` (16-byte aligned rows) a whole row moves as
+// eight 16-byte loads instead of 32 scattered ones.
 template <bool UPPER>
-__device__ __forceinline__ void load_row(const float *A, int64_t lda, int i, int k0, int kend, float (&v)[32]) {
+__device__ __forceinline__ void load_row(const float *A, int64_t lda, int i, int k0, int kend, float (&v)[32],
+                                         bool vec) {
+    if (UPPER && vec && kend >= k0 + 32) {
+        const float4 *p = reinterpret_cast<const float4 *>(A + static_cast<int64_t>(i) * lda + k0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 t = p[q];
+            v[4 * q + 0] = t.x;
+            v[4 * q + 1] = t.y;
+            v[4 * q + 2] = t.z;
+            v[4 * q + 3] = t.w;
+        }
+        return;
+    }
 #pragma unroll
     for (int c = 0; c < 32; ++c) v[c] = (k0 + c < kend) ? A[sidx<UPPER>(i, k0 + c, lda)] : 0.f;
 }
@@ -202,9 +218,16 @@ __device__ __forceinline__ void invert_diag(int lane, const float *sLs, const fl
     for (int k = 24; k < 32; ++k) invert_step<8>(acc, lane, k, sLs, sRs, b_hi, b_lo);
 }
 
-// S(i, k0 + c) = v[c] for c < cend.
+// S(i, k0 + c) = v[c] for c < cend (Upper with `vec` and a whole row: eight 16-byte stores).
 template <bool UPPER>
-__device__ __forceinline__ void store_row(float *A, int64_t lda, int i, int k0, int cend, const float (&v)[32]) {
+__device__ __forceinline__ void store_row(float *A, int64_t lda, int i, int k0, int cend, const float (&v)[32],
+                                          bool vec) {
+    if (UPPER && vec && cend == 32) {
+        float4 *p = reinterpret_cast<float4 *>(A + static_cast<int64_t>(i) * lda + k0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) p[q] = make_float4(v[4 * q + 0], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        return;
+    }
 #pragma unroll
     for (int c = 0; c < 32; ++c)
         if (c < cend) A[sidx<UPPER>(i, k0 + c, lda)] = v[c];
@@ -233,6 +256,9 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
     const int n = args.n;
     float *A = static_cast<T *>(args.A) + mat * args.stride_a;
     const int64_t lda = args.lda;
+    // 16-byte aligned rows of S (Upper): aligned base and item stride, lda a multiple of 4
+    const bool vec = UPPER && (lda % 4 == 0) && (args.stride_a % 4 == 0) &&
+                     ((reinterpret_cast<uintptr_t>(args.A) & 15) == 0);
     if (args.mode != MODE_POTRF) return;      // factor-only variant (the dispatcher never asks otherwise)
 
     if (warp == 0) {
@@ -282,11 +308,10 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
         // ---------------------------------------------- 1. block update from the finished columns
         const int nk = C0 >> 5;
         if (nk > 0) {
-            float xa[32], xb[32];
-            colblk::load_row<UPPER>(A, lda, C0 + rA, 0, rA < M ? 32 : 0, xa);
-            colblk::load_row<UPPER>(A, lda, C0 + rB, 0, rB < M ? 32 : 0, xb);
-            // double-buffered: chunk kc goes to panel kc&1 while the MMAs of chunk kc-1 run
-            for (int kc = 0; kc < nk; ++kc) {
+            // chunk kc is staged into panel kc&1 while the MMAs of chunk kc-1 run; each chunk's
+            // rows are loaded two chunks ahead into one of two register buffers, so the global
+            // load latency overlaps a whole chunk step
+            auto step = [&](int kc, const float (&xa)[32], const float (&xb)[32]) {
                 const int pb = kc & 1;
                 wait_mma(pb);                                // chunk kc-2's MMAs are done: panel pb is free
                 unsigned char *bh = sm + (pb ? C::P1_HI : C::P0_HI), *bl = sm + (pb ? C::P1_LO : C::P0_LO);
@@ -296,7 +321,7 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
                 tc::fence_before_sync();
                 __syncthreads();
                 tc::fence_after_sync();
-                if (s_stop) { stop = true; break; }          // uniform: read after the barrier
+                if (s_stop) { stop = true; return; }         // uniform: read after the barrier
                 if (tid == 0) {
                     const uint32_t ph = s_base + static_cast<uint32_t>(pb ? C::P1_HI : C::P0_HI);
                     const uint32_t pl = s_base + static_cast<uint32_t>(pb ? C::P1_LO : C::P0_LO);
@@ -306,9 +331,22 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
                     tc::mma_commit(&s_mbar[pb]);
                 }
                 pend |= 1u << pb;
-                if (kc + 1 < nk) {                           // next chunk's loads overlap these MMAs
-                    colblk::load_row<UPPER>(A, lda, C0 + rA, 32 * (kc + 1), rA < M ? 32 * (kc + 2) : 0, xa);
-                    colblk::load_row<UPPER>(A, lda, C0 + rB, 32 * (kc + 1), rB < M ? 32 * (kc + 2) : 0, xb);
+            };
+            auto fetch = [&](int kc, float (&xa)[32], float (&xb)[32]) {
+                colblk::load_row<UPPER>(A, lda, C0 + rA, 32 * kc, rA < M ? 32 * (kc + 1) : 0, xa, vec);
+                colblk::load_row<UPPER>(A, lda, C0 + rB, 32 * kc, rB < M ? 32 * (kc + 1) : 0, xb, vec);
+            };
+            float xa0[32], xb0[32], xa1[32], xb1[32];
+            fetch(0, xa0, xb0);
+            if (nk > 1) fetch(1, xa1, xb1);
+            for (int kc = 0; kc < nk && !stop; kc += 2) {
+                step(kc, xa0, xb0);
+                if (stop) break;
+                if (kc + 2 < nk) fetch(kc + 2, xa0, xb0);
+                if (kc + 1 < nk) {
+                    step(kc + 1, xa1, xb1);
+                    if (stop) break;
+                    if (kc + 3 < nk) fetch(kc + 3, xa1, xb1);
                 }
             }
         }
@@ -320,8 +358,8 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
             const int rlo = 32 * q;                          // the slice's diagonal rows start here
             const bool liveA = rA >= rlo && rA < M, liveB = rB < M;
             float va[32], vb[32];
-            colblk::load_row<UPPER>(A, lda, C0 + rA, Q0, liveA ? Q0 + kq : 0, va);
-            colblk::load_row<UPPER>(A, lda, C0 + rB, Q0, liveB ? Q0 + kq : 0, vb);
+            colblk::load_row<UPPER>(A, lda, C0 + rA, Q0, liveA ? Q0 + kq : 0, va, vec);
+            colblk::load_row<UPPER>(A, lda, C0 + rB, Q0, liveB ? Q0 + kq : 0, vb, vec);
             wait_mma(0);
             wait_mma(1);
             if (C0 > 0 || q > 0) {                           // the accumulator holds this slice's update
@@ -391,8 +429,8 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
             const bool xA = tA < mtiles && (warp >= 4 || warp > q), xB = tB < mtiles;   // warp-uniform
             if (xA) tc::tmem_ld32(tmem + lane_base + static_cast<uint32_t>(tA * 128 + 32 * q), va);
             if (xB) tc::tmem_ld32(tmem + lane_base + static_cast<uint32_t>(tB * 128 + 32 * q), vb);
-            if (solA) colblk::store_row<UPPER>(A, lda, C0 + rA, Q0, kq, va);
-            if (liveB) colblk::store_row<UPPER>(A, lda, C0 + rB, Q0, kq, vb);
+            if (solA) colblk::store_row<UPPER>(A, lda, C0 + rA, Q0, kq, va, vec);
+            if (liveB) colblk::store_row<UPPER>(A, lda, C0 + rB, Q0, kq, vb, vec);
             if (next) {
                 if (solA) colblk::panel_row(p_hi, p_lo, rA, va);
                 if (liveB) colblk::panel_row(p_hi, p_lo, rB, vb);

@@ -97,7 +97,7 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     } else {
         if constexpr (WHOLE && C::full_ok && C::smem_solve_full <= 227 * 1024) {
             if (full) {
-                auto kern = warp_kernel<T, P, R, true, 1, true>;
+                auto kern = warp_kernel<T, P, R, true, 1, true, PK>;
                 static std::atomic<unsigned long long> done{0};
                 cudaError_t e = ensure_smem(kern, C::smem_solve_full, done);
                 if (e != cudaSuccess) return e;
@@ -105,7 +105,7 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
                 return cudaGetLastError();
             }
         }
-        auto kern = warp_kernel<T, P, R, true, 1>;
+        auto kern = warp_kernel<T, P, R, true, 1, false, PK>;
         static std::atomic<unsigned long long> done{0};
         cudaError_t e = ensure_smem(kern, C::smem_solve, done);
         if (e != cudaSuccess) return e;
