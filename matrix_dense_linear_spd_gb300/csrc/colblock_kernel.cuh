@@ -189,11 +189,20 @@ __device__ __forceinline__ void invert_step(float (&acc)[32], int lane, int k, c
 // right-looking, one column per step in a compact loop over the full-width frame. (A frame that
 // narrows with the finished columns measured slower here: the chain is latency-bound, and the
 // extra loop boundaries cost more than the FMAs they save.) Returns the failure bit mask.
-__device__ __forceinline__ unsigned factor_diag(float (&a)[32], int lane, int kq, float *sLs, float *sRs) {
+//
+// After column j is published, the column count `ready` becomes base + j + 1 (a block-scope
+// release), so a second warp can invert the block one column behind.
+__device__ __forceinline__ unsigned factor_diag(float (&a)[32], int lane, int kq, float *sLs, float *sRs, int *ready,
+                                                int base) {
     unsigned failed = 0;
     float d = __shfl_sync(0xffffffffu, a[0], 0);
 #pragma unroll 1
-    for (int j = 0; j < 32; ++j) factor_step<32>(a, lane, j, kq, d, failed, sLs, sRs);
+    for (int j = 0; j < 32; ++j) {
+        factor_step<32>(a, lane, j, kq, d, failed, sLs, sRs);
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) *reinterpret_cast<volatile int *>(ready) = base + j + 1;
+    }
     return failed;
 }
 
@@ -203,19 +212,46 @@ __device__ __forceinline__ unsigned factor_diag(float (&a)[32], int lane, int kq
 // index c of a 32-row operand tile, so the tile holds Linv row by row (the B operand of
 // X = V * Linv^T). The frame narrows by 8 every 8 steps (32, 24, 16, 8 live rows), so no work is
 // spent on rows already finished.
-__device__ __forceinline__ void invert_diag(int lane, const float *sLs, const float *sRs, unsigned char *b_hi,
-                                            unsigned char *b_lo) {
+//
+// Runs on a second warp while the factor is still in progress: before step k it waits (bounded)
+// until the column count `ready` exceeds base + k. Returns false if a wait gave up.
+__device__ __forceinline__ bool wait_column(const int *ready, int target, uint32_t max_polls) {
+    for (uint32_t i = 0; i < max_polls; ++i) {
+        if (*reinterpret_cast<const volatile int *>(ready) > target) {
+            __threadfence_block();
+            return true;
+        }
+    }
+    return false;
+}
+
+__device__ __forceinline__ bool invert_diag(int lane, const float *sLs, const float *sRs, unsigned char *b_hi,
+                                            unsigned char *b_lo, const int *ready, int base) {
+    constexpr uint32_t kPolls = 1u << 22;
     float acc[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] = (i == lane) ? 1.f : 0.f;
 #pragma unroll 1
-    for (int k = 0; k < 8; ++k) invert_step<32>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+    for (int k = 0; k < 8; ++k) {
+        if (!wait_column(ready, base + k, kPolls)) return false;
+        invert_step<32>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+    }
 #pragma unroll 1
-    for (int k = 8; k < 16; ++k) invert_step<24>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+    for (int k = 8; k < 16; ++k) {
+        if (!wait_column(ready, base + k, kPolls)) return false;
+        invert_step<24>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+    }
 #pragma unroll 1
-    for (int k = 16; k < 24; ++k) invert_step<16>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+    for (int k = 16; k < 24; ++k) {
+        if (!wait_column(ready, base + k, kPolls)) return false;
+        invert_step<16>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+    }
 #pragma unroll 1
-    for (int k = 24; k < 32; ++k) invert_step<8>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+    for (int k = 24; k < 32; ++k) {
+        if (!wait_column(ready, base + k, kPolls)) return false;
+        invert_step<8>(acc, lane, k, sLs, sRs, b_hi, b_lo);
+    }
+    return true;
 }
 
 // S(i, k0 + c) = v[c] for c < cend (Upper with `vec` and a whole row: eight 16-byte stores).
@@ -250,6 +286,7 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
     __shared__ uint64_t s_mbar[2];                 // MMA completion, per operand panel
     __shared__ int s_stop;     // 0 running, 2 a bounded wait gave up
     __shared__ int s_diag;     // failing column of the current diagonal block, -1 none
+    __shared__ int s_ready;    // diagonal-block columns published so far (all slices)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t mat = blockIdx.x;
@@ -270,6 +307,7 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
         tc::mbar_init(&s_mbar[1], 1);
         tc::mbar_fence_init();
         s_stop = 0;
+        s_ready = 0;
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -298,6 +336,7 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
     const int rA = tid, rB = tid + 256;
     const int tA = warp >> 2, tB = 2 + (warp >> 2);
     bool stop = false;
+    int slice_no = 0;
 
     for (int C0 = 0; C0 < n && !stop; C0 += C::W) {
         const int M = n - C0;
@@ -384,26 +423,31 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
                 }
             }
             const bool solA = rA >= rlo + 32 && rA < M;     // rows below the diagonal block
-            // diagonal block: warp q holds its rows (lane l = row Q0 + l); padding rows are identity.
-            // It factors them, stores them, and inverts L11 into the B tile of the solve.
+            // diagonal block: warp q holds its rows (lane l = row Q0 + l; padding rows are identity),
+            // factors and stores them; warp 4 + (q+1)%4 (on another scheduler) inverts L11 into the
+            // B tile of the solve one column behind; the other rows go, split, into the panel (the
+            // A operand of the solve)
+            const int base = 32 * slice_no++;
             if (warp == q) {
                 if (liveB) colblk::panel_row(p_hi, p_lo, rB, vb);   // this warp's lower rows first
                 float a[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) a[c] = (lane < kq) ? (c <= lane ? va[c] : 0.f) : (c == lane ? 1.f : 0.f);
-                const unsigned failed = colblk::factor_diag(a, lane, kq, sLs, sRs);
-                __syncwarp();
+                const unsigned failed = colblk::factor_diag(a, lane, kq, sLs, sRs, &s_ready, base);
                 // the diagonal block's lower part (columns before a failure are final)
                 if (lane < kq) {
 #pragma unroll 1
                     for (int c = 0; c <= lane; ++c) A[colblk::sidx<UPPER>(Q0 + lane, Q0 + c, lda)] = sLs[c * 32 + lane - c];
                 }
-                colblk::invert_diag(lane, sLs, sRs, sm + C::OFF_BI_HI, sm + C::OFF_BI_LO);
                 if (lane == 0) s_diag = failed ? __ffs(failed) - 1 : -1;
+            } else {
+                if (solA) colblk::panel_row(p_hi, p_lo, rA, va);
+                if (liveB) colblk::panel_row(p_hi, p_lo, rB, vb);
+                if (warp == 4 + ((q + 1) & 3)) {
+                    if (!colblk::invert_diag(lane, sLs, sRs, sm + C::OFF_BI_HI, sm + C::OFF_BI_LO, &s_ready, base))
+                        s_stop = 2;
+                }
             }
-            // meanwhile the rows below go, split, into the panel: the A operand of the solve
-            if (solA) colblk::panel_row(p_hi, p_lo, rA, va);
-            if (liveB && warp != q) colblk::panel_row(p_hi, p_lo, rB, vb);
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncthreads();
