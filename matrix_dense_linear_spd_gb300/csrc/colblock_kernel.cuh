@@ -42,8 +42,9 @@ struct ColBlkCfg {
     static constexpr int MAXN = 512;                                // 4 row tiles x 128 tensor-memory columns
     // operand panels: rows x 32 tf32 (128 bytes), hi and lo parts. Panel 0 holds up to MAXN rows
     // (the slices of the first block); panel 1, the second buffer of the block update, up to
-    // MAXN - W rows (blocks after the first). The diagonal block's L columns and reciprocal
-    // pivots live in panel 1's space: the slices never use panel 1.
+    // MAXN - W rows (blocks after the first). The diagonal block's L columns, its reciprocal
+    // pivots and its inverse (the B tile of the panel solve) live in panel 1's space: the slices
+    // never use panel 1, and no block-update MMA is in flight while a slice runs.
     static constexpr size_t P0_HI = 0;
     static constexpr size_t P0_LO = static_cast<size_t>(MAXN) * 128;
     static constexpr size_t P1_HI = 2 * P0_LO;
