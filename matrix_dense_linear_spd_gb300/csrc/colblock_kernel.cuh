@@ -127,40 +127,51 @@ __device__ __forceinline__ void mma_k32(uint32_t d, uint32_t a_hi, uint32_t a_lo
     }
 }
 
-// One step of the diagonal-block factor in a shifting frame of F live columns: a[0] is the
-// current column j, a[m] column j+m. Publishes L(j+m, j) to sLs[j*32 + m] and 1/L(j,j) to
-// sRs[j]; the next column takes L(j+1, j) by a shuffle, and the next pivot itself,
-// A(j+1,j+1) - L(j+1,j)^2, is formed by its own lane and broadcast into d; the rest of the update
-// reads the published column back as 16-byte broadcasts (positions past the block hold stale
-// values and only touch entries past the block). (Each further shuffle on this chain measured
-// slower than the shared-memory path it replaces.)
-template <int F>
-__device__ __forceinline__ void factor_step(float (&a)[32], int lane, int j, int kq, float &d, unsigned &failed,
-                                            float *sLs, float *sRs) {
+// One step j of the diagonal-block factor (lane = row) in a shifting register frame: on entry
+// a[m] is column j+m of this lane's row, updated by every column before j except column j-1's
+// contribution to columns j+3 and beyond, which is applied here ("delayed") from column j-1 as
+// published in shared memory (cvp[m] = L(j-1+m, j-1)) and this lane's lp = L(lane, j-1). The
+// pivot chain never waits on shared memory: L(j+1, j) and L(j+2, j) come by shuffles, and the
+// next pivot, A(j+1,j+1) - L(j+1,j)^2, is formed by its own lane and broadcast into d. The delayed
+// FMAs depend only on the previous step, so they fill the chain's latency. On exit the frame has
+// moved by one column. Column j of L goes to sLs[j*32 + m] = L(j+m, j), 1/L(j,j) to sRs[j].
+template <bool FIRST>
+__device__ __forceinline__ void factor_step(float (&a)[32], float &lp, int lane, int j, int kq, float &d,
+                                            unsigned &failed, float *sLs, float *sRs) {
+    float cvp[32];
+    if (FIRST) {
+#pragma unroll
+        for (int m = 0; m < 32; ++m) cvp[m] = 0.f;
+    } else {
+        const float4 *c4 = reinterpret_cast<const float4 *>(sLs + (j - 1) * 32);
+#pragma unroll
+        for (int m4 = 0; m4 < 8; ++m4) {
+            const float4 v4 = c4[m4];
+            cvp[4 * m4 + 0] = v4.x;
+            cvp[4 * m4 + 1] = v4.y;
+            cvp[4 * m4 + 2] = v4.z;
+            cvp[4 * m4 + 3] = v4.w;
+        }
+    }
     const bool ok = d > 0.f;
     const float rs = ok ? rsqrtf(d) : 0.f;
     failed |= (ok || j >= kq) ? 0u : (1u << j);
     const float l = (lane == j) ? (ok ? d * rs : d) : (lane > j ? a[0] * rs : 0.f);
     if (lane >= j) sLs[j * 32 + (lane - j)] = l;
     if (lane == 0) sRs[j] = rs;
+    const float l1 = __shfl_sync(0xffffffffu, l, (j + 1) & 31);   // L(j+1, j); 0 past the block
+    const float l2 = __shfl_sync(0xffffffffu, l, (j + 2) & 31);   // L(j+2, j)
     d = __shfl_sync(0xffffffffu, fmaf(-l, l, a[1]), (j + 1) & 31);   // lane j+1: its next pivot
-    const float l1 = __shfl_sync(0xffffffffu, l, (j + 1) & 31);
-    const float a0 = fmaf(-l, l1, a[1]);
-    __syncwarp();
-    const float4 *c4 = reinterpret_cast<const float4 *>(sLs + j * 32);
+    const float n0 = fmaf(-l, l1, a[1]);
+    const float n1 = fmaf(-l, l2, fmaf(-lp, cvp[3], a[2]));
 #pragma unroll
-    for (int m4 = 0; m4 < (F + 3) / 4; ++m4) {
-        const float4 v4 = c4[m4];
-        const float cv[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int m = 4 * m4 + e;
-            if (m < 2 || m >= F) continue;
-            a[m - 1] = fmaf(-l, cv[e], a[m]);              // column j+m -= L(lane, j) * L(j+m, j)
-        }
-    }
-    a[0] = a0;
-    a[F - 1] = 0.f;
+    for (int p = 2; p < 30; ++p) a[p] = fmaf(-lp, cvp[p + 2], a[p + 1]);   // column j+1+p, delayed
+    a[30] = a[31];                                   // column j+31: valid only for j = 0 (lp = 0)
+    a[31] = 0.f;
+    a[0] = n0;
+    a[1] = n1;
+    lp = l;
+    __syncwarp();                                    // column j is published for the next step
 }
 
 // One step of the inverse (column `lane` of Linv, shifting frame of F live rows): acc[0] is row
@@ -187,22 +198,22 @@ __device__ __forceinline__ void invert_step(float (&acc)[32], int lane, int k, c
 }
 
 // Factor the 32 x 32 diagonal block held by one warp (lane = row; padding rows are identity),
-// right-looking, one column per step in a compact loop over the full-width frame. (A frame that
-// narrows with the finished columns measured slower here: the chain is latency-bound, and the
-// extra loop boundaries cost more than the FMAs they save.) Returns the failure bit mask.
-//
-// After column j is published, the column count `ready` becomes base + j + 1 (a block-scope
-// release), so a second warp can invert the block one column behind.
+// right-looking, one column per step in a compact loop (the step above). Returns the failure bit
+// mask. Every 4 columns (and after the last) the column count `ready` becomes base + j + 1 (a
+// block-scope release), so a second warp can invert the block a few columns behind.
 __device__ __forceinline__ unsigned factor_diag(float (&a)[32], int lane, int kq, float *sLs, float *sRs, int *ready,
                                                 int base) {
     unsigned failed = 0;
+    float lp = 0.f;
     float d = __shfl_sync(0xffffffffu, a[0], 0);
+    factor_step<true>(a, lp, lane, 0, kq, d, failed, sLs, sRs);
 #pragma unroll 1
-    for (int j = 0; j < 32; ++j) {
-        factor_step<32>(a, lane, j, kq, d, failed, sLs, sRs);
-        __threadfence_block();
-        __syncwarp();
-        if (lane == 0) *reinterpret_cast<volatile int *>(ready) = base + j + 1;
+    for (int j = 1; j < 32; ++j) {
+        factor_step<false>(a, lp, lane, j, kq, d, failed, sLs, sRs);
+        if ((j & 3) == 3 && lane == 0) {
+            __threadfence_block();
+            *reinterpret_cast<volatile int *>(ready) = base + j + 1;
+        }
     }
     return failed;
 }
@@ -222,6 +233,7 @@ __device__ __forceinline__ bool wait_column(const int *ready, int target, uint32
             __threadfence_block();
             return true;
         }
+        __nanosleep(32);                             // keep the polling off the shared-memory pipe
     }
     return false;
 }
@@ -435,11 +447,6 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
 #pragma unroll
                 for (int c = 0; c < 32; ++c) a[c] = (lane < kq) ? (c <= lane ? va[c] : 0.f) : (c == lane ? 1.f : 0.f);
                 const unsigned failed = colblk::factor_diag(a, lane, kq, sLs, sRs, &s_ready, base);
-                // the diagonal block's lower part (columns before a failure are final)
-                if (lane < kq) {
-#pragma unroll 1
-                    for (int c = 0; c <= lane; ++c) A[colblk::sidx<UPPER>(Q0 + lane, Q0 + c, lda)] = sLs[c * 32 + lane - c];
-                }
                 if (lane == 0) s_diag = failed ? __ffs(failed) - 1 : -1;
             } else {
                 if (solA) colblk::panel_row(p_hi, p_lo, rA, va);
@@ -453,7 +460,16 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
             tc::fence_before_sync();
             __syncthreads();
             tc::fence_after_sync();
+            // the diagonal block's lower part, from its published columns (columns before a failure
+            // are final), stored by warp q; after the solve's MMAs are issued when there is no failure
+            auto store_diag = [&]() {
+                if (warp == q && lane < kq) {
+#pragma unroll 1
+                    for (int c = 0; c <= lane; ++c) A[colblk::sidx<UPPER>(Q0 + lane, Q0 + c, lda)] = sLs[c * 32 + lane - c];
+                }
+            };
             if (s_stop || s_diag >= 0) {                     // uniform: read after the barrier
+                store_diag();
                 if (tid == 0 && !s_stop) args.info[mat] = Q0 + s_diag + 1;
                 stop = true;
                 break;
@@ -469,6 +485,7 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
                 tc::mma_commit(&s_mbar[0]);
             }
             pend |= 1u;
+            store_diag();
             wait_mma(0);
             const bool next = 32 * (q + 1) < Wb;             // the block has further slices
             const bool xA = tA < mtiles && (warp >= 4 || warp > q), xB = tB < mtiles;   // warp-uniform
