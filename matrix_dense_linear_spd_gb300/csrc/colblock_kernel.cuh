@@ -491,8 +491,6 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
             const bool xA = tA < mtiles && (warp >= 4 || warp > q), xB = tB < mtiles;   // warp-uniform
             if (xA) tc::tmem_ld32(tmem + lane_base + static_cast<uint32_t>(tA * 128 + 32 * q), va);
             if (xB) tc::tmem_ld32(tmem + lane_base + static_cast<uint32_t>(tB * 128 + 32 * q), vb);
-            if (solA) colblk::store_row<UPPER>(A, lda, C0 + rA, Q0, kq, va, vec);
-            if (liveB) colblk::store_row<UPPER>(A, lda, C0 + rB, Q0, kq, vb, vec);
             if (next) {
                 if (solA) colblk::panel_row(p_hi, p_lo, rA, va);
                 if (liveB) colblk::panel_row(p_hi, p_lo, rB, vb);
@@ -518,6 +516,9 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
                 __syncthreads();                             // L11 and the panel are free again
                 tc::fence_after_sync();
             }
+            // the solved rows go to global memory while the tensor cores run the update above
+            if (solA) colblk::store_row<UPPER>(A, lda, C0 + rA, Q0, kq, va, vec);
+            if (liveB) colblk::store_row<UPPER>(A, lda, C0 + rB, Q0, kq, vb, vec);
         }
     }
     wait_mma(0);
