@@ -404,7 +404,11 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
         for (int j = 0; j < N; ++j) {
             // columns >= n are identity padding: skipping them is exact, and the uniform branch
             // keeps the scheduler from interleaving all N unrolled steps (which costs registers)
-            if (j >= n) break;
+            if (FULL && PK) {
+                asm volatile("" ::: "memory");            // n = N: a scheduling fence instead of the exit test
+            } else if (j >= n) {
+                break;
+            }
             const int rj = j / P, lj = j - rj * P;
             const Rt d = __shfl_sync(0xffffffffu, re(a[rj][j]), g * P + lj);
             T *col = colbuf + (j & 1) * CBX;
