@@ -404,8 +404,10 @@ __global__ void __launch_bounds__(128, MINB) warp_kernel(const BatchArgs args) {
         for (int j = 0; j < N; ++j) {
             // columns >= n are identity padding: skipping them is exact, and the uniform branch
             // keeps the scheduler from interleaving all N unrolled steps (which costs registers)
-            if (FULL && PK) {
-                asm volatile("" ::: "memory");            // n = N: a scheduling fence instead of the exit test
+            // n = N with whole squares: an empty asm fence replaces the exit test where the
+            // registers allow (the scheduler may then overlap neighbouring columns a little)
+            if (FULL && PK && (SOLVE || R <= 2)) {
+                asm volatile("" ::: "memory");
             } else if (j >= n) {
                 break;
             }
