@@ -220,3 +220,29 @@ def test_shipped_tables_name_only_compiled_variants(bl):
                     times.append(float(parts[1]))
             assert times == sorted(times) or len(times) < 2 or max(times) / min(times) < 1.5, (f, line)
         assert keys_seen, f
+
+
+def test_column_block_and_packed_routes_parse_and_select(bl):
+    """The column-block tensor-core variant (blocked:nb=32:tc=2, f32 potrf, n <= 512) and the
+    packed-FMA lane-row variants (warp:...:x2=1, f32) are compiled, pinnable by their spellings,
+    refused where they cannot run, and chosen by the shipped f32 tables where they were fastest."""
+    f32 = {sp: (cap, rhs) for sp, cap, rhs in bl.routes("f32")}
+    assert f32["blocked:nb=32:tc=2"] == (512, -1)                  # factor only, n <= 512
+    for sp in ("warp:p=16:r=2:full=1:x2=1", "warp:p=8:r=4:full=1:x2=1", "warp:p=8:r=2:full=1:x2=1"):
+        assert sp in f32, sp
+    for other in ("f64", "c64", "c128"):
+        assert not any(sp.endswith(":x2=1") or sp.endswith(":tc=2") for sp, _, _ in bl.routes(other))
+    for op, sp, n, ok in (("potrf", "blocked:nb=32:tc=2", 512, True), ("potrf", "blocked:nb=32:tc=2", 513, False),
+                          ("posv", "blocked:nb=32:tc=2", 64, False), ("potrf", "warp:p=16:r=2:full=1:x2=1", 32, True),
+                          ("potrf", "WARP:16:2:1:1", 32, True), ("posv", "warp:p=8:r=4:full=1:x2=1", 28, True)):
+        bl.set_route(op, sp)
+        try:
+            out = bl.select_debug(op, "f32", "L", n, 4 if op == "posv" else 0, 64)
+            assert out.startswith("error:") != ok, (op, sp, n, out)
+        finally:
+            bl.set_route(op, None)
+    # the shipped tables route the benchmark shape and the large orders to the new variants
+    assert bl.select_debug("potrf", "f32", "L", 32, 0, 16384).startswith("warp:p=16:r=2:full=1:x2=1")
+    assert bl.select_debug("potrf", "f32", "L", 512, 0, 1024).startswith("blocked:nb=32:tc=2")
+    assert bl.select_debug("potrf", "f32", "U", 512, 0, 1024).startswith("blocked:nb=32:tc=2")
+    assert bl.select_debug("posv", "f32", "L", 512, 8, 1024).startswith("blocked:nb=32 ")
