@@ -66,7 +66,8 @@ inline unsigned persistent_grid(K kern, int threads, size_t smem, int64_t ctas_n
 // WHOLE: the "full=1" variant, which copies whole squares into its slabs when the call's items are
 // stored back to back (n = N, lda = N, stride = N*N, 16-byte aligned) and otherwise runs the
 // compacted-triangle kernel like the plain variant (same arithmetic, bit-identical results).
-// PK: packed two-lane FP32 FMAs in the factor-only kernel (f32; the solve kernel is shared).
+// PK: packed two-lane FP32 FMAs in the rank-1 update (f32), in both the factor-only and the
+// solve kernels.
 template <typename T, int P, int R, bool WHOLE = false, bool PK = false>
 cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     using C = WarpCfg<T, P, R>;
