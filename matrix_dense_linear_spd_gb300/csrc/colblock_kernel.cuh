@@ -284,7 +284,6 @@ __device__ __forceinline__ void store_row(float *A, int64_t lda, int i, int k0, 
 
 }  // namespace colblk
 
-
 template <typename T, bool UPPER>
 __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) {
     static_assert(sizeof(T) == 4 && !is_cplx<T>::value, "column-block tensor-core kernel: f32");
