@@ -1,34 +1,34 @@
 """Benchmark: batched potrf throughput on the f32 n=32 batch=16384 workload (Lower).
 
 One step = one bl_potrf call over the whole batch (pivot, scale, trailing update, load and
-store of every item), inputs resident in HBM. The operation is in place, so before every
-timed step the input is restored from a pristine device copy and L2 is flushed (both
-untimed); the step itself is timed with CUDA events on the launching stream.
+store of every item), inputs resident in HBM. The operation is in place, so every step factors
+its own pristine copy of the batch: steps run back to back in chunks (CUDA events around each
+chunk on the launching stream), the copies of a chunk together exceed four times the L2 size,
+and they are restored and L2 flushed before each chunk, untimed (protocol.py).
 
 Printed JSON line (one per run, rank 0):
   value        matrices/s over all ranks (weak scaling: every rank factors its own batch)
   e2e          the same metric through the public C ABI with the batch in pinned host memory:
                host->device copy, bl_potrf, device->host copy of the factor and info, per step
+               (two streams alternate, so copies overlap the other step's kernel)
   roofline     achieved algorithmic GB/s of the potrf kernel against the measured HBM copy
                bandwidth (MEASURED_PEAKS.json); algorithmic bytes = the referenced triangle read
                and written at 32-byte sector granularity plus the 4-byte info per item
   cpu_baseline the CPU oracle (long double) on the host cores, on a bounded sample
-  also         Upper potrf and posv (nrhs = 4) on the same batch, same protocol
+  also         Upper potrf, posv (nrhs = 4), one isolated call, and cuSOLVER potrfBatched on the
+               same batch and protocol (vendor reference point)
 
 --impl reference times the CPU oracle alone on the same workload (the reference arm).
 """
 from __future__ import annotations
 
 import argparse
-import ctypes
 import hashlib
 import json
 import math
 import os
 import statistics
-import subprocess
 import sys
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -70,107 +70,7 @@ def potrf_flops(n: int, dtype: str) -> float:
     return n ** 3 / 3 + n ** 2 / 2 + n / 6
 
 
-# ------------------------------------------------------------------ clocks (NVML via ctypes)
-
-class ClockSampler:
-    """Samples SM clock and clock-event reasons every few ms in a background thread."""
-    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
-               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
-
-    def __init__(self, torch_device: int = 0, period: float = 0.005):
-        self.period = period
-        self.samples = []
-        self.max_mhz = None
-        self.ok = False
-        self._stop = threading.Event()
-        try:
-            import torch
-            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
-            if self.nvml.nvmlInit_v2() != 0:
-                raise OSError("nvmlInit failed")
-            self.handle = ctypes.c_void_p()
-            uuid = None
-            try:
-                uuid = str(torch.cuda.get_device_properties(torch_device).uuid)
-            except Exception:
-                pass
-            rc = 1
-            if uuid:
-                for cand in (uuid, "GPU-" + uuid):
-                    rc = self.nvml.nvmlDeviceGetHandleByUUID(cand.encode(), ctypes.byref(self.handle))
-                    if rc == 0:
-                        break
-            if rc != 0:
-                rc = self.nvml.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.handle))
-            if rc != 0:
-                raise OSError("no NVML handle")
-            m = ctypes.c_uint()
-            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(m)) == 0:
-                self.max_mhz = m.value
-            self.ok = True
-        except Exception:
-            self.ok = False
-
-    def _one(self):
-        c = ctypes.c_uint()
-        r = ctypes.c_ulonglong()
-        if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(c)) != 0:
-            return
-        self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.handle, ctypes.byref(r))
-        self.samples.append((time.perf_counter(), c.value, r.value))
-
-    def _run(self):
-        while not self._stop.is_set():
-            self._one()
-            time.sleep(self.period)
-
-    def start(self):
-        if self.ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
-        return self
-
-    def stop(self):
-        if self.ok:
-            self._stop.set()
-            self._t.join()
-
-    def summary(self, t0=None, t1=None):
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
-                    "source": "nvml unavailable"}
-        sel = [s for s in self.samples if (t0 is None or s[0] >= t0) and (t1 is None or s[0] <= t1)]
-        if len(sel) < 3:
-            sel = self.samples
-        reasons = set()
-        for _, _, r in sel:
-            for bit, name in self.REASONS.items():
-                if r & bit:
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(s[1] for s in sel), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(reasons), "samples": len(sel), "source": "nvml"}
-
-
 # ------------------------------------------------------------------ helpers
-
-class L2Flush:
-    """Evict L2 between timed steps: write one buffer larger than L2, then read a second one,
-    so the lines left in L2 are clean and no write-back of the flush lands in the timed
-    kernel."""
-
-    def __init__(self, l2_bytes: int, device):
-        import torch
-        n = max(2 * l2_bytes, 256 << 20) // 4
-        self.a = torch.empty(n, dtype=torch.float32, device=device)
-        self.b = torch.ones(n, dtype=torch.float32, device=device)
-        self.sink = torch.empty((), dtype=torch.float32, device=device)
-        self.mib = n * 4 >> 20
-
-    def zero_(self):
-        self.a.zero_()
-        import torch
-        torch.sum(self.b, dim=0, out=self.sink)
-
 
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -226,22 +126,42 @@ def dist_env():
     return ws, rank, local
 
 
-def cpu_oracle_rate(w, uplo: str, target_s: float = 8.0, max_items: int = 4096):
-    """Oracle matrices/s on the host cores over a bounded leading sample of the workload."""
+def host_cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_oracle_rate(w, uplo: str, target_s: float = 8.0, max_items: int = 4096, reps: int = 3):
+    """Oracle matrices/s on the host cores over a bounded leading sample of the workload:
+    the sample is sized by one calibration run to about target_s / reps of wall time, then
+    timed `reps` times; the median is reported."""
     import oracle
     cores = os.cpu_count() or 1
     n = w.n
     k = min(max(cores, 64), w.batch)
-    t = 0.0
+    per_run = target_s / max(reps, 1)
     while True:
         buf = synth.to_colmajor(w.A[:k])
         t0 = time.perf_counter()
         oracle.run(uplo, n, k, buf, n, n * n, threads=cores)
         t = time.perf_counter() - t0
-        if t >= target_s or k >= min(max_items, w.batch):
+        if t >= per_run or k >= min(max_items, w.batch):
             break
-        k = min(min(max_items, w.batch), max(k * 2, int(k * target_s / max(t, 1e-3))))
-    return k / t, k, t, cores
+        k = min(min(max_items, w.batch), max(k * 2, int(k * per_run / max(t, 1e-3))))
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.run(uplo, n, k, buf, n, n * n, threads=cores)
+        ts.append(time.perf_counter() - t0)
+    t = statistics.median(ts)
+    return k / t, k, t, cores, oracle.long_double_digits()
 
 
 # ------------------------------------------------------------------ the GPU arm
@@ -249,6 +169,8 @@ def cpu_oracle_rate(w, uplo: str, target_s: float = 8.0, max_items: int = 4096):
 def run_ours(args, ws, rank, local):
     import torch
     import matrix_dense_linear_spd_gb300 as bl
+    from matrix_dense_linear_spd_gb300 import protocol as P
+    from matrix_dense_linear_spd_gb300.clocks import ClockSampler
 
     torch.cuda.set_device(local)
     dist = None
@@ -262,129 +184,138 @@ def run_ours(args, ws, rank, local):
     w = synth.workload(args.workload)
     n, batch, dtype = w.n, w.batch, w.dtype
     code = bl.DTYPE_CODES[dtype]
+    esz = ESIZE[dtype]
     buf = synth.to_colmajor(w.A)
     pristine = torch.from_numpy(buf).to(dev)
-    work = pristine.clone()
-    info = torch.empty(batch, dtype=torch.int32, device=dev)
+    item_bytes = pristine.numel() * pristine.element_size()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
-    flusher = L2Flush(l2, dev)
-    flush = flusher
+    flush = P.L2Flush(l2, dev)
+    R = P.copies_per_chunk(item_bytes, l2, args.steps)
+    rot = P.Rotation([pristine], R)
+    infos = torch.zeros((R, batch), dtype=torch.int32, device=dev)
 
-    def potrf_once(uplo):
-        bl.potrf_ptr(uplo, code, n, batch, work.data_ptr(), n, n * n, info.data_ptr(), sptr)
+    def potrf_call(uplo):
+        return lambda i: bl.potrf_ptr(uplo, code, n, batch, rot.ptr(0, i), n, n * n, infos[i].data_ptr(), sptr)
 
-    nrhs = w.nrhs or 4
-    Bp = torch.from_numpy(synth.to_colmajor(w.B if w.B is not None else
-                                            synth.rhs_uniform(np.random.default_rng(9), n, nrhs, batch, dtype))).to(dev)
-    Bw = Bp.clone()
-
-    def posv_once(uplo):
-        bl.posv_ptr(uplo, code, n, nrhs, batch, work.data_ptr(), n, n * n, Bw.data_ptr(), n, n * nrhs,
-                    info.data_ptr(), sptr)
-
-    def timed(fn, uplo, steps, warmup, restore_b=False):
-        for _ in range(warmup):
-            work.copy_(pristine)
-            if restore_b:
-                Bw.copy_(Bp)
-            flush.zero_()
-            fn(uplo)
-        torch.cuda.synchronize()
-        evs = []
-        for _ in range(steps):
-            work.copy_(pristine)
-            if restore_b:
-                Bw.copy_(Bp)
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn(uplo)
-            e1.record(stream)
-            evs.append((e0, e1))
-        torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in evs]
-
-    # untimed: first call selects and configures, then a clock-warming phase
-    potrf_once("L")
+    call_l = potrf_call("L")
+    # untimed: the first call selects and configures; then a clock-warming phase
+    rot.restore()
+    call_l(0)
     torch.cuda.synchronize()
     route = bl.last_choice()
     sampler = ClockSampler(local).start()
     t_end = time.perf_counter() + args.warm_seconds
     while time.perf_counter() < t_end:
-        for _ in range(20):
-            work.copy_(pristine)
-            potrf_once("L")
+        rot.restore()
+        for i in range(R):
+            call_l(i)
         torch.cuda.synchronize()
 
+    # ---- the timed region: exactly `steps` calls, back to back on distinct pristine copies
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    ms = timed(potrf_once, "L", args.steps, args.warmup)
+    per_call, total_ms = P.time_back_to_back(call_l, rot, flush, args.steps, stream,
+                                             warm_chunks=max(1, math.ceil(args.warmup / R)))
     t1 = time.perf_counter()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.stop()
-    ms_step = sum(ms) / len(ms)
+    ms_step = total_ms / args.steps
     ms_max, value = aggregate(ms_step, batch, dist, dev)
-    ok_info = int(info.abs().sum().item()) == 0
+    ok_info = int(infos.abs().sum().item()) == 0
+    st_main = P.stats(per_call)
 
-    # extras on the same batch: Upper potrf and posv
     also = {}
     if not args.no_extras:
-        msu = timed(potrf_once, "U", args.steps, 2)
+        # one call on its own (restore, L2 flush, events around the single call)
+        iso = P.time_isolated(call_l, rot, flush, 30, stream)
+        also["potrf_lower_isolated_call"] = {"ms_per_call": P.stats(iso)["median"], "rel_sd": P.stats(iso)["rel_sd"],
+                                             "protocol": "restore + L2 flush, then events around one call; median of 30"}
+        # Upper on the same batch
+        call_u = potrf_call("U")
+        pu, tu = P.time_back_to_back(call_u, rot, flush, args.steps, stream)
         route_u = bl.last_choice()
-        msp = timed(posv_once, "L", args.steps, 2, restore_b=True)
-        route_p = bl.last_choice()
+        msu = tu / args.steps
         bu = potrf_bytes(n, dtype, "U")
-        # vendor reference point: cuSOLVER batched potrf through torch.linalg.cholesky_ex
-        # (out of place: its time includes torch's copy of the input into the output)
-        Acm = work.view(batch, n, n)
-        vend = {}
-        for up in (False, True):
-            for _ in range(3):
-                torch.linalg.cholesky_ex(Acm, upper=up, check_errors=False)
-            vt = []
-            for _ in range(max(10, args.steps // 4)):
-                work.copy_(pristine)
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                torch.linalg.cholesky_ex(Acm, upper=up, check_errors=False)
-                e1.record(stream)
-                vt.append((e0, e1))
-            torch.cuda.synchronize()
-            ms_v = statistics.median(a.elapsed_time(b) for a, b in vt)
-            vend["upper" if up else "lower"] = {"matrices_per_s": batch / (ms_v / 1e3), "ms_per_call": ms_v}
-        also = {
-            "cusolver_potrf_via_torch": vend,
-            "potrf_upper": {"matrices_per_s": batch / (statistics.mean(msu) / 1e3),
-                            "ms_per_call": statistics.mean(msu), "route": route_u,
-                            "gbs": bu * batch / (statistics.mean(msu) / 1e3) / 1e9},
-            "posv_nrhs%d" % nrhs: {"matrices_per_s": batch / (statistics.mean(msp) / 1e3),
-                                   "ms_per_call": statistics.mean(msp), "route": route_p},
-        }
+        also["potrf_upper"] = {"matrices_per_s": batch / (msu / 1e3), "ms_per_call": msu, "route": route_u,
+                               "gbs": bu * batch / (msu / 1e3) / 1e9, "rel_sd": P.stats(pu)["rel_sd"]}
+        # posv with nrhs right-hand sides (A and B restored together)
+        nrhs = w.nrhs or 4
+        Bh = w.B if w.B is not None else synth.rhs_uniform(np.random.default_rng(9), n, nrhs, batch, dtype)
+        Bp = torch.from_numpy(synth.to_colmajor(Bh)).to(dev)
+        rot2 = P.Rotation([pristine, Bp], R)
+        posv = lambda i: bl.posv_ptr("L", code, n, nrhs, batch, rot2.ptr(0, i), n, n * n, rot2.ptr(1, i), n,
+                                     n * nrhs, infos[i].data_ptr(), sptr)
+        pp, tp = P.time_back_to_back(posv, rot2, flush, args.steps, stream)
+        route_p = bl.last_choice()
+        msp = tp / args.steps
+        also["posv_nrhs%d" % nrhs] = {"matrices_per_s": batch / (msp / 1e3), "ms_per_call": msp, "route": route_p,
+                                      "rel_sd": P.stats(pp)["rel_sd"]}
+        del rot2
+        # vendor reference point: cuSOLVER potrfBatched, in place, pointer arrays built untimed,
+        # same protocol; then ours again (second pass, reversed order) to expose drift
+        try:
+            from matrix_dense_linear_spd_gb300.vendor import CusolverPotrfBatched
+            cus = CusolverPotrfBatched()
+            ptrs = [cus.pointer_array(rot.ptr(0, i), batch, n * n, dtype, dev) for i in range(R)]
+            vend = {}
+            for up in ("L", "U"):
+                vcall = lambda i, up=up: cus.potrf(up, dtype, n, batch, ptrs[i], n, infos[i].data_ptr(), sptr)
+                pv, tv = P.time_back_to_back(vcall, rot, flush, args.steps, stream)
+                msv = tv / args.steps
+                vend["lower" if up == "L" else "upper"] = {"matrices_per_s": batch / (msv / 1e3), "ms_per_call": msv,
+                                                          "rel_sd": P.stats(pv)["rel_sd"],
+                                                          "info_all_zero": int(infos.abs().sum().item()) == 0}
+            cus.close()
+            also["cusolver_potrfBatched"] = vend
+        except Exception as e:  # the reference point is context; its absence is reported
+            also["cusolver_potrfBatched"] = {"unavailable": str(e)[:200]}
+        p2, t2 = P.time_back_to_back(call_l, rot, flush, args.steps, stream)
+        also["potrf_lower_second_pass"] = {"ms_per_call": t2 / args.steps, "rel_sd": P.stats(p2)["rel_sd"],
+                                           "vs_first_pass": (t2 / args.steps) / ms_step}
+    del rot
 
-    # e2e through the C ABI with pinned host buffers
+    # ---- e2e through the C ABI with pinned host buffers: every step copies its batch in, factors
+    # it and copies the factor and info out; two streams alternate so one step's copies overlap
+    # the other's work, as a caller streaming batches would run it
     host_in = torch.from_numpy(buf).pin_memory()
-    host_out = torch.empty_like(host_in).pin_memory()
-    host_info = torch.empty(batch, dtype=torch.int32).pin_memory()
-    e2e_ms = []
-    for it in range(args.warmup + args.steps):
-        flush.zero_()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        work.copy_(host_in, non_blocking=True)
-        potrf_once("L")
-        host_out.copy_(work, non_blocking=True)
-        host_info.copy_(info, non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if it >= args.warmup:
-            e2e_ms.append(e0.elapsed_time(e1))
-    e2e_step, _ = aggregate(statistics.mean(e2e_ms), batch, dist, dev)
+    host_out = [torch.empty_like(host_in).pin_memory() for _ in range(2)]
+    host_info = [torch.empty(batch, dtype=torch.int32).pin_memory() for _ in range(2)]
+    dbuf = [torch.empty_like(pristine) for _ in range(2)]
+    dinfo = [torch.empty(batch, dtype=torch.int32, device=dev) for _ in range(2)]
+    streams = [torch.cuda.Stream(dev) for _ in range(2)]
+
+    def e2e_step(k):
+        s_ = streams[k & 1]
+        with torch.cuda.stream(s_):
+            dbuf[k & 1].copy_(host_in, non_blocking=True)
+            bl.potrf_ptr("L", code, n, batch, dbuf[k & 1].data_ptr(), n, n * n, dinfo[k & 1].data_ptr(), s_.cuda_stream)
+            host_out[k & 1].copy_(dbuf[k & 1], non_blocking=True)
+            host_info[k & 1].copy_(dinfo[k & 1], non_blocking=True)
+
+    for k in range(args.warmup):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    flush()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s_ in streams:
+        s_.wait_event(e0)
+    for k in range(args.steps):
+        e2e_step(k)
+    for s_ in streams:
+        ev = torch.cuda.Event()
+        ev.record(s_)
+        stream.wait_event(ev)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_info_ok = all(int(h.abs().sum().item()) == 0 for h in host_info)
+    e2e_step_max, _ = aggregate(e2e_ms, batch, dist, dev)
 
     peaks, peak_src = measured_peaks()
     alg_bytes = potrf_bytes(n, dtype, "L") * batch
@@ -396,27 +327,38 @@ def run_ours(args, ws, rank, local):
         "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded SPD batch, A = B*B^T + n*I)",
         "config": {"workload": f"potrf {dtype} Lower n={n} batch={batch} (seed 1)",
                    "lda": n, "stride": n * n, "route": route,
-                              "l2": "flushed before every step: write of %d MiB then read of another %d MiB (L2 left clean); input restored untimed" % (flusher.mib, flusher.mib),
+                   "l2": (f"inputs larger than L2: each step factors its own pristine copy of the batch; chunks of "
+                          f"{R} back-to-back steps ({R * item_bytes >> 20} MiB of inputs, L2 {l2 >> 20} MiB), "
+                          f"copies restored and L2 flushed ({flush.mib} MiB write + read) before each chunk, untimed"),
                    "parallelism": f"weak: {ws} independent batches"},
+        "timing": {"per_step_ms_median": st_main["median"], "rel_sd": st_main["rel_sd"], "chunks": st_main["n"],
+                   "steps_per_chunk": R, "noisy": st_main["rel_sd"] > 0.10},
         "gbs": alg_bytes * ws / (ms_max / 1e3) / 1e9,
-        "gbs_full_storage": (2 * n * n * ESIZE[dtype] + 4) * batch * ws / (ms_max / 1e3) / 1e9,
+        "gbs_full_storage": (2 * n * n * esz + 4) * batch * ws / (ms_max / 1e3) / 1e9,
         "gflops": potrf_flops(n, dtype) * batch * ws / (ms_max / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": recorded_traffic(kernel_tag),
                      "algorithmic_bytes_per_launch": alg_bytes, "kernel": kernel_tag,
-                     "peak_source": f"{peak_src} (copy bandwidth, burst)"},
-        "e2e": {"value": ws * batch / (e2e_step / 1e3), "unit": UNIT,
+                     "peak_source": f"{peak_src} (copy bandwidth, burst: of measured)"},
+        "e2e": {"value": ws * batch / (e2e_step_max / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
-                "d2h_bytes_per_step": host_out.numel() * host_out.element_size() + host_info.numel() * 4},
+                "d2h_bytes_per_step": host_out[0].numel() * host_out[0].element_size() + batch * 4,
+                "info_all_zero": e2e_info_ok,
+                "protocol": "pinned host buffers; per step: H2D of the batch, bl_potrf, D2H of factor and info; "
+                            "two streams alternate (copies of one step overlap the other's kernel); events around "
+                            "all steps"},
         "gpu_launches": args.steps,
         "clocks": sampler.summary(t0 - args.warm_seconds, t1),
         "info_all_zero": ok_info,
         "also": also,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rate, k, t, cores = cpu_oracle_rate(w, "L", target_s=args.cpu_seconds)
+        rate, k, t, cores, ldig = cpu_oracle_rate(w, "L", target_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"first {k} items of the workload, {t:.1f} s wall"}
+                                "sample": f"first {k} items of the workload, median of 3 runs ({t:.2f} s each)",
+                                "cpu": host_cpu_model(),
+                                "long_double": {64: "x87 80-bit extended", 113: "IEEE binary128 (software)"}.get(
+                                    ldig, f"{ldig}-bit mantissa")}
     if dist:
         dist.destroy_process_group()
     return line if rank == 0 else None
@@ -424,30 +366,32 @@ def run_ours(args, ws, rank, local):
 
 def run_reference(args):
     """The reference arm: the CPU oracle on the host cores, each step a bounded sample."""
-    import oracle  # noqa: F401
+    import oracle
     w = synth.workload(args.workload)
     cores = os.cpu_count() or 1
-    rate0, k, t, _ = cpu_oracle_rate(w, "L", target_s=min(args.cpu_seconds, 3.0), max_items=2048)
+    rate0, k, t, _, ldig = cpu_oracle_rate(w, "L", target_s=min(args.cpu_seconds, 3.0), max_items=2048, reps=1)
     per_step = max(1, min(w.batch, int(rate0 * args.reference_step_seconds)))
     buf = synth.to_colmajor(w.A[:per_step])
-    import oracle as orc
     for _ in range(args.warmup):
-        orc.run("L", w.n, per_step, buf, w.n, w.n * w.n, threads=cores)
+        oracle.run("L", w.n, per_step, buf, w.n, w.n * w.n, threads=cores)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        orc.run("L", w.n, per_step, buf, w.n, w.n * w.n, threads=cores)
+        oracle.run("L", w.n, per_step, buf, w.n, w.n * w.n, threads=cores)
         times.append(time.perf_counter() - t0)
-    ms = 1e3 * statistics.mean(times)
+    ms = 1e3 * sum(times) / len(times)
     value = per_step / (ms / 1e3)
+    fmt = {64: "x87 80-bit extended", 113: "IEEE binary128 (software)"}.get(ldig, f"{ldig}-bit mantissa")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": f"potrf {w.dtype} Lower n={w.n} batch={w.batch} (seed 1)",
                    "sample_per_step": per_step},
+        "timing": {"per_step_ms_median": 1e3 * statistics.median(times)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{per_step} items per step (leading items of the workload)"},
+                         "sample": f"{per_step} items per step (leading items of the workload)",
+                         "cpu": host_cpu_model(), "long_double": fmt},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -144,13 +144,34 @@ const char *bl_select_debug(int op, bl_dtype dtype, bl_uplo uplo, int64_t n, int
 
 /*
  * Diagnostic: one 128 x 128 tile C = A * B^T on the tensor cores (tcgen05, kind::tf32) with the
- * 3xTF32 split the blocked factorisation's trailing update uses. A and B are device pointers to
+ * 3xTF32 split the column-block factorisation's updates use. A and B are device pointers to
  * 128 x 32 row-major f32 matrices, C to a 128 x 128 row-major f32 result; *status (device int32,
  * initially 0) becomes 1 on completion or 2 if the tensor-core work did not complete within the
  * kernel's bounded wait. Launches one CTA on `stream`.
  */
 bl_status bl_debug_tc_tile_f32(const float *A, const float *B, float *C, int32_t *status,
                                bl_stream_t stream);
+
+/*
+ * Diagnostic: arithmetic-peak microbenchmarks, so that roofline fractions can be taken against
+ * rates measured on the device in use (the pages state their rooflines against measured
+ * bandwidths and rates of the card under test: "Small-n baseline", the DRAM-roof paragraph).
+ * Launches `blocks` CTAs of one kernel that keeps one execution unit busy for `iters` loop trips
+ * and stores the kernel's total flop count in *flops (host pointer); the caller times the launch
+ * (CUDA events on `stream`) and divides. `scratch` is a device buffer of at least 2 KB that the
+ * kernels never write in practice (it keeps the arithmetic from being optimised away); *status
+ * (device int32, initially 0) becomes 2 if a tensor-core kernel's bounded wait for its MMAs gave
+ * up. Kinds:
+ *   BL_PEAK_FFMA   FP32 fma.rn.f32, 256-thread CTAs         BL_PEAK_FFMA2  FP32 fma.rn.f32x2 pairs
+ *   BL_PEAK_DFMA   FP64 fma                                 BL_PEAK_DMMA   FP64 mma.sync m16n8k4
+ *   BL_PEAK_TF32   tcgen05.mma kind::tf32, 128x256x8, one CTA per SM (blocks = SM count)
+ *   BL_PEAK_BF16   tcgen05.mma kind::f16 (bf16), 128x256x16, one CTA per SM
+ */
+typedef enum {
+    BL_PEAK_FFMA = 0, BL_PEAK_FFMA2 = 1, BL_PEAK_DFMA = 2, BL_PEAK_DMMA = 3, BL_PEAK_TF32 = 4, BL_PEAK_BF16 = 5
+} bl_peak_kind;
+bl_status bl_debug_peak(int kind, int blocks, int iters, void *scratch, int32_t *status, double *flops,
+                        bl_stream_t stream);
 
 #ifdef __cplusplus
 }

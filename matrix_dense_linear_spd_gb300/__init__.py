@@ -24,7 +24,7 @@ STATUS = {0: "success", 1: "invalid argument", 2: "no route", 3: "CUDA error", 4
 
 EXPORTED = ("bl_potrf", "bl_posv", "bl_potrs", "bl_status_string", "bl_last_error", "bl_last_choice",
             "bl_version", "bl_set_route", "bl_num_routes", "bl_route_name", "bl_route_capacity",
-            "bl_select_debug", "bl_debug_tc_tile_f32")
+            "bl_select_debug", "bl_debug_tc_tile_f32", "bl_debug_peak")
 
 
 class BLError(RuntimeError):
@@ -62,6 +62,8 @@ def _load():
     lib.bl_select_debug.restype = ctypes.c_char_p
     lib.bl_debug_tc_tile_f32.argtypes = [vp, vp, vp, vp, vp]
     lib.bl_debug_tc_tile_f32.restype = ctypes.c_int
+    lib.bl_debug_peak.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, ctypes.POINTER(ctypes.c_double), vp]
+    lib.bl_debug_peak.restype = ctypes.c_int
     return lib
 
 

@@ -522,7 +522,11 @@ __global__ void __launch_bounds__(256, 1) colblock_kernel(const BatchArgs args) 
     }
     wait_mma(0);
     wait_mma(1);
-    if (lost >= 0) tc::mbar_wait(&s_mbar[lost], (phase >> lost) & 1u, kPolls);  // once more for the batch given up on
+    // A thread whose wait gave up polls once more for that batch (no MMA was issued after it gave
+    // up: the issuing thread reads s_stop after the next barrier). The outcome is published
+    // through shared memory behind a barrier, so every thread takes the same path below; the item
+    // reports -1 whenever any wait gave up, and the tensor memory is released either way.
+    if (lost >= 0 && !tc::mbar_wait(&s_mbar[lost], (phase >> lost) & 1u, kPolls)) s_stop = 2;
     __syncthreads();
     if (tid == 0) {
         if (s_stop == 2) args.info[mat] = -1;

@@ -25,6 +25,7 @@
 #include <mutex>
 #include <sstream>
 #include <string>
+#include <tuple>
 #include <vector>
 
 #include "registry.h"
@@ -57,19 +58,35 @@ const char *dtype_name(int d) {
     return (d >= 0 && d < 4) ? names[d] : "?";
 }
 
-std::vector<const KernelEntry *> candidates(int dtype) {
-    int count = 0;
-    const KernelEntry *e = nullptr;
-    switch (dtype) {
-        case BL_F32: e = bl::entries_f32(&count); break;
-        case BL_F64: e = bl::entries_f64(&count); break;
-        case BL_C64: e = bl::entries_c64(&count); break;
-        case BL_C128: e = bl::entries_c128(&count); break;
-        default: break;
-    }
-    std::vector<const KernelEntry *> v;
-    for (int i = 0; i < count; ++i) v.push_back(e + i);
-    return v;
+std::string spelling(const KernelEntry &e);
+
+// The compiled variants of a dtype with their spellings, built once.
+struct Candidates {
+    std::vector<const KernelEntry *> e;
+    std::vector<std::string> sp;
+};
+
+const Candidates &candidates(int dtype) {
+    static std::once_flag once;
+    static Candidates all[4];
+    std::call_once(once, [] {
+        for (int d = 0; d < 4; ++d) {
+            int count = 0;
+            const KernelEntry *e = nullptr;
+            switch (d) {
+                case BL_F32: e = bl::entries_f32(&count); break;
+                case BL_F64: e = bl::entries_f64(&count); break;
+                case BL_C64: e = bl::entries_c64(&count); break;
+                default: e = bl::entries_c128(&count); break;
+            }
+            for (int i = 0; i < count; ++i) {
+                all[d].e.push_back(e + i);
+                all[d].sp.push_back(spelling(e[i]));
+            }
+        }
+    });
+    static const Candidates none;
+    return (dtype >= 0 && dtype < 4) ? all[dtype] : none;
 }
 
 std::string spelling(const KernelEntry &e) {
@@ -78,7 +95,7 @@ std::string spelling(const KernelEntry &e) {
     else if (e.family == 2)   // nb bit 0: whole squares, bit 1: packed f32x2 update
         snprintf(buf, sizeof buf, "warp:p=%d:r=%d%s%s", e.p, e.s, (e.nb & 1) ? ":full=1" : "", (e.nb & 2) ? ":x2=1" : "");
     else if (e.family == 3) snprintf(buf, sizeof buf, "thread:n=%d", e.nb);
-    else if (e.s) snprintf(buf, sizeof buf, "blocked:nb=%d:tc=%d", e.nb, e.s);   // tensor-core update (1: trailing, 2: column block)
+    else if (e.s) snprintf(buf, sizeof buf, "blocked:nb=%d:tc=%d", e.nb, e.s);   // 2: the column-block tensor-core kernel
     else snprintf(buf, sizeof buf, "blocked:nb=%d", e.nb);
     return buf;
 }
@@ -304,15 +321,17 @@ std::string env_pin(int op) {
 
 bl_status choose_on(const DeviceFacts &dev, int op, int dtype, int uplo, int64_t n, int64_t nrhs,
                     int64_t batch, Choice &out) {
-    const auto cands = candidates(dtype);
+    const Candidates &cs = candidates(dtype);
+    const auto &cands = cs.e;
     std::string pin;
     auto tp = t_pins.find(op_name(op));
     if (tp != t_pins.end() && !tp->second.empty()) pin = tp->second;
     else pin = env_pin(op);
     std::string cp = canon(pin);
     if (!cp.empty() && cp != "auto") {
-        for (const KernelEntry *e : cands)
-            if (spelling(*e) == cp) {
+        for (size_t i = 0; i < cands.size(); ++i)
+            if (cs.sp[i] == cp) {
+                const KernelEntry *e = cands[i];
                 if (!can_run(*e, op, n, nrhs, dev))
                     return fail(BL_ERR_INVALID_ARGUMENT, "%s route pin '%s' cannot run %s n=%lld nrhs=%lld",
                                 op_name(op), pin.c_str(), dtype_name(dtype), (long long)n, (long long)nrhs);
@@ -331,8 +350,9 @@ bl_status choose_on(const DeviceFacts &dev, int op, int dtype, int uplo, int64_t
         if (op != OP_POTRF) lg["nrhs"] = double(nrhs);
         if (const Row *r = nearest_row(*t, ex, lg)) {
             for (const std::string &sp : r->ranked)
-                for (const KernelEntry *e : cands)
-                    if (spelling(*e) == sp && can_run(*e, op, n, nrhs, dev)) {
+                for (size_t i = 0; i < cands.size(); ++i)
+                    if (cs.sp[i] == sp && can_run(*cands[i], op, n, nrhs, dev)) {
+                        const KernelEntry *e = cands[i];
                         char buf[160];
                         snprintf(buf, sizeof buf, "table %s row n=%g batch=%g", tag.c_str(),
                                  r->logk.count("n") ? r->logk.at("n") : 0.0,
@@ -361,10 +381,38 @@ bl_status choose_on(const DeviceFacts &dev, int op, int dtype, int uplo, int64_t
     return BL_SUCCESS;
 }
 
+// Resolved choices, per thread, keyed by everything the choice depends on (device, op, dtype,
+// uplo, n, nrhs, batch and the pin in force): a repeated call skips the table search.
+struct ChoiceKey {
+    int dev, op, dtype, uplo;
+    int64_t n, nrhs, batch;
+    std::string pin;
+    bool operator<(const ChoiceKey &o) const {
+        return std::tie(dev, op, dtype, uplo, n, nrhs, batch, pin) <
+               std::tie(o.dev, o.op, o.dtype, o.uplo, o.n, o.nrhs, o.batch, o.pin);
+    }
+};
+thread_local std::map<ChoiceKey, Choice> t_choice_cache;
+
 bl_status choose(int op, int dtype, int uplo, int64_t n, int64_t nrhs, int64_t batch, Choice &out) {
+    int devno = 0;
+    if (cudaGetDevice(&devno) != cudaSuccess) return fail(BL_ERR_CUDA, "cannot query the current CUDA device");
+    auto tp = t_pins.find(op_name(op));
+    ChoiceKey key{devno, op, dtype, uplo, n, op == OP_POTRF ? 0 : nrhs, batch,
+                  (tp != t_pins.end() && !tp->second.empty()) ? tp->second : env_pin(op)};
+    auto hit = t_choice_cache.find(key);
+    if (hit != t_choice_cache.end()) {
+        out = hit->second;
+        return BL_SUCCESS;
+    }
     DeviceFacts dev;
     if (!device_facts(dev)) return fail(BL_ERR_CUDA, "cannot query the current CUDA device");
-    return choose_on(dev, op, dtype, uplo, n, nrhs, batch, out);
+    bl_status st = choose_on(dev, op, dtype, uplo, n, nrhs, batch, out);
+    if (st == BL_SUCCESS) {
+        if (t_choice_cache.size() > 4096) t_choice_cache.clear();
+        t_choice_cache[key] = out;
+    }
+    return st;
 }
 
 bool trace_on() {
@@ -524,23 +572,23 @@ const char *bl_select_debug(int op, bl_dtype dtype, bl_uplo uplo, int64_t n, int
 
 // Number of compiled kernel variants for a dtype, and the spelling of variant i (for sweeps
 // and tests). Returns NULL when i is out of range.
-int bl_num_routes(bl_dtype dtype) { return static_cast<int>(candidates(dtype).size()); }
+int bl_num_routes(bl_dtype dtype) { return static_cast<int>(candidates(dtype).e.size()); }
 
 const char *bl_route_name(bl_dtype dtype, int i) {
     static thread_local std::string s;
-    auto c = candidates(dtype);
-    if (i < 0 || i >= static_cast<int>(c.size())) return nullptr;
-    s = spelling(*c[i]);
+    const auto &c = candidates(dtype);
+    if (i < 0 || i >= static_cast<int>(c.e.size())) return nullptr;
+    s = c.sp[i];
     return s.c_str();
 }
 
 // Capacity of variant i: the largest n + rhs-per-pass it holds (0 = any) and the right-hand
 // sides it solves per pass (0 = any). Returns -1 when i is out of range.
 int bl_route_capacity(bl_dtype dtype, int i, int *rhs_per_pass_out) {
-    auto c = candidates(dtype);
-    if (i < 0 || i >= static_cast<int>(c.size())) return -1;
-    if (rhs_per_pass_out) *rhs_per_pass_out = c[i]->rhs_max;
-    return c[i]->cap;
+    const auto &c = candidates(dtype);
+    if (i < 0 || i >= static_cast<int>(c.e.size())) return -1;
+    if (rhs_per_pass_out) *rhs_per_pass_out = c.e[i]->rhs_max;
+    return c.e[i]->cap;
 }
 
 }  // extern "C"

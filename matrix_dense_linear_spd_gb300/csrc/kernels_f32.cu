@@ -41,7 +41,6 @@ static const KernelEntry k_entries_f32[] = {
     tile_entry<float, 16, 10>(),
     blocked_entry<float, 32>(),
     blocked_entry<float, 64>(),
-    blocked_entry<float, 32, true>(),
     colblock_entry<float>(),
 };
 

@@ -3,6 +3,9 @@
 
 #include <atomic>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <cuda_runtime.h>
 
 #include "bl_types.cuh"
@@ -40,26 +43,41 @@ cudaError_t launch_tile(const BatchArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <typename T, int NB, bool TC = false>
+template <typename T, int NB>
 cudaError_t launch_blocked(const BatchArgs &a, cudaStream_t st) {
-    using C = BlkCfg<T, NB, TC>;
+    using C = BlkCfg<T, NB>;
     static std::atomic<unsigned long long> done{0};
-    cudaError_t e = ensure_smem(blocked_kernel<T, NB, TC>, C::smem_bytes, done);
+    cudaError_t e = ensure_smem(blocked_kernel<T, NB>, C::smem_bytes, done);
     if (e != cudaSuccess) return e;
-    blocked_kernel<T, NB, TC><<<static_cast<unsigned>(a.batch), C::THREADS, C::smem_bytes, st>>>(a);
+    blocked_kernel<T, NB><<<static_cast<unsigned>(a.batch), C::THREADS, C::smem_bytes, st>>>(a);
     return cudaGetLastError();
 }
 
 // Persistent grid for the warp family: enough CTAs to fill every SM at the kernel's occupancy,
-// never more than the work needs.
+// never more than the work needs. The resident-CTA count is cached per kernel, device and
+// shared-memory size (the occupancy query costs more than the launch itself).
 template <typename K>
 inline unsigned persistent_grid(K kern, int threads, size_t smem, int64_t ctas_needed) {
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
-        per_sm = 1, sms = sms > 0 ? sms : 1;
-    const int64_t full = static_cast<int64_t>(sms) * per_sm;
+    static std::mutex mu;
+    static std::map<std::tuple<const void *, int, size_t>, long long> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    const auto key = std::make_tuple(reinterpret_cast<const void *>(kern), dev, smem);
+    long long full = 0;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) full = it->second;
+    }
+    if (full <= 0) {
+        int sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
+            per_sm = 1, sms = sms > 0 ? sms : 1;
+        full = static_cast<long long>(sms) * per_sm;
+        std::lock_guard<std::mutex> lk(mu);
+        cache[key] = full;
+    }
     return static_cast<unsigned>(ctas_needed < full ? ctas_needed : full);
 }
 
@@ -96,7 +114,7 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         kern<<<persistent_grid(kern, C::THREADS, sm, ctas), C::THREADS, sm, st>>>(a);
     } else {
-        if constexpr (WHOLE && C::full_ok && C::smem_solve_full <= 227 * 1024) {
+        if constexpr (WHOLE && C::full_solve_ok && C::smem_solve_full <= 227 * 1024) {
             if (full) {
                 auto kern = warp_kernel<T, P, R, true, 1, true, PK>;
                 static std::atomic<unsigned long long> done{0};
@@ -168,12 +186,10 @@ constexpr KernelEntry colblock_entry() {
                        &launch_colblock<T>};
 }
 
-template <typename T, int NB, bool TC = false>
+template <typename T, int NB>
 constexpr KernelEntry blocked_entry() {
-    using C = BlkCfg<T, NB, TC>;
-    // the tensor-core variant keeps the whole L21 panel in shared memory: n <= TC_MAXM + NB
-    return KernelEntry{1, 0, TC ? 1 : 0, NB, TC ? C::TC_MAXM + NB : 0, 0, C::THREADS, 1, C::smem_bytes,
-                       &launch_blocked<T, NB, TC>};
+    using C = BlkCfg<T, NB>;
+    return KernelEntry{1, 0, 0, NB, 0, 0, C::THREADS, 1, C::smem_bytes, &launch_blocked<T, NB>};
 }
 
 }  // namespace bl

@@ -1,6 +1,6 @@
 // Diagnostic: one 128 x 128 output tile C = A * B^T (A, B: 128 x 32, f32, row-major) on the
 // tensor cores with the 3xTF32 split (hi*hi + hi*lo + lo*hi), through exactly the descriptors,
-// tensor-memory handling and completion protocol the blocked Cholesky's trailing update uses.
+// tensor-memory handling and completion protocol the column-block Cholesky's updates use.
 // It exists so that layer can be checked in isolation against a host product.
 #include <cuda_runtime.h>
 

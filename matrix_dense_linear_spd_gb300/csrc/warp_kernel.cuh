@@ -125,6 +125,10 @@ struct WarpCfg {
     static constexpr size_t smem_full = off_col_full + (col_bytes + 15) / 16 * 16;
     static constexpr bool full_ok = sizeof(T) <= 8 && (N * N / E) % 32 == 0 && (P * sizeof(T)) % 16 == 0 &&
                                     (FSTRIDE * sizeof(T)) % 16 == 0;
+    // the solve kernel on whole squares keeps the rows, the right-hand sides and the slab
+    // addresses live at once; above 128 words of rows per lane it no longer fits 255 registers
+    // (ptxas spills), so those geometries solve from the compacted slab
+    static constexpr bool full_solve_ok = full_ok && row_words() <= 128;
     static constexpr size_t smem_potrf = off_stage + stage_bytes;
     static constexpr size_t smem_solve = off_x + x_bytes;
     static constexpr size_t full_shift = off_col_full - off_col;   // solve areas move up by this
@@ -158,23 +162,33 @@ __device__ __forceinline__ int lower_slab_offset(int c) {
 
 // Copy one group's contiguous run of whole squares into the slab with column stride NS: chunk k
 // (16 bytes) is matrix k / CPM, column (k mod CPM) / CPCOL, chunk k mod CPCOL of that column.
+// Only the chunks that meet the referenced triangle move (Lower: chunk q of column c when it
+// holds a row >= c; Upper: when it holds a row <= c), so HBM delivers the triangle's sectors and
+// not the whole square; the slab positions of the other chunks keep stale values, which only
+// reach register entries on the other side of the diagonal (never read into the factor).
 // When 32 lanes span whole columns every offset but the lane's is an immediate.
-template <typename T, int NS, int CPM, int CPCOL, int IT, int FSTRIDE, int E>
+template <typename T, bool UPPER, int NS, int CPM, int CPCOL, int IT, int FSTRIDE, int E>
 __device__ __forceinline__ void full_copy(T *tri, const T *src, int lane, int64_t mleft) {
     if constexpr (32 % CPCOL == 0) {
         T *dst = tri + (lane / CPCOL) * NS + (lane % CPCOL) * E;
+        // the lane's chunk q = lane % CPCOL in column c = c0 + lane / CPCOL is needed when
+        // (Lower) q*E + E - 1 >= c, i.e. c0 <= dl, or (Upper) q*E <= c, i.e. c0 >= du
+        const int dl = (lane % CPCOL) * E + E - 1 - lane / CPCOL;
+        const int du = (lane % CPCOL) * E - lane / CPCOL;
 #pragma unroll
         for (int it = 0; it < IT; ++it) {
             const int gg = (32 * it) / CPM;
             const int c0 = (32 * it - gg * CPM) / CPCOL;
-            if (gg < mleft) cp_async_16(dst + gg * FSTRIDE + c0 * NS, src + 32 * it * E);
+            const bool need = UPPER ? (c0 >= du) : (c0 <= dl);
+            if (gg < mleft && need) cp_async_16(dst + gg * FSTRIDE + c0 * NS, src + 32 * it * E);
         }
     } else {
 #pragma unroll
         for (int it = 0; it < IT; ++it) {
             const int k = lane + 32 * it;
             const int gg = k / CPM, w = k - gg * CPM, c = w / CPCOL, q = w - c * CPCOL;
-            if (gg < mleft) cp_async_16(tri + gg * FSTRIDE + c * NS + q * E, src + 32 * it * E);
+            const bool need = UPPER ? (q * E <= c) : (q * E + E - 1 >= c);
+            if (gg < mleft && need) cp_async_16(tri + gg * FSTRIDE + c * NS + q * E, src + 32 * it * E);
         }
     }
 }
@@ -199,8 +213,8 @@ __device__ __forceinline__ void warp_prefetch(const BatchArgs &args, T *tri, int
         constexpr int IT = G * CPM / 32;
         static_assert((G * CPM) % 32 == 0 && CPM % 32 == 0, "whole chunks per lane");
         const T *src = A0 + lane * E;
-        if (upper) full_copy<T, C::NS, CPM, CPCOL, IT, C::FSTRIDE, E>(tri, src, lane, mleft);
-        else full_copy<T, C::NS_L, CPM, CPCOL, IT, C::FSTRIDE, E>(tri, src, lane, mleft);
+        if (upper) full_copy<T, true, C::NS, CPM, CPCOL, IT, C::FSTRIDE, E>(tri, src, lane, mleft);
+        else full_copy<T, false, C::NS_L, CPM, CPCOL, IT, C::FSTRIDE, E>(tri, src, lane, mleft);
         cp_async_commit();
         return;
     }

@@ -1,15 +1,22 @@
-"""Per-workload report: every named synthetic workload measured with the benchmark protocol
-(input restored and L2 flushed before each call, CUDA events around the call, trimmed mean
-of the middle 60% of the repetitions), with
-matrices/s, GB/s, GFLOP/s and the achieved fraction of the binding roof, next to cuSOLVER's
-batched potrf (through torch.linalg.cholesky_ex) as a reference point.
+"""Per-workload report: every named synthetic workload measured with the benchmark's protocol
+(protocol.py: back-to-back calls on distinct pristine copies, inputs larger than four times L2,
+CUDA events around each chunk; plus one isolated call after an L2 flush), with matrices/s, GB/s,
+GFLOP/s and the achieved fraction of the binding roof, next to cuSOLVER's batched potrf
+(cusolverDn<t>potrfBatched, in place, pointer arrays built untimed) as a reference point. The
+vendor and library arms run interleaved chunk by chunk, in alternating order.
 
-Roofs: HBM copy bandwidth from MEASURED_PEAKS.json; FP32 and FP64 from unit counts at the
-maximum SM clock (152 SMs x 128 FP32 lanes x 2 flops, and x 2 FP64 lanes x 2 flops, per clock).
-The binding roof of a workload is the larger of bytes/HBM and flops/FP peak.
+Roofs, all measured on the GPU the report runs on:
+  HBM   the copy bandwidth in MEASURED_PEAKS.json;
+  FP32  max(FFMA, packed FFMA2) from profiles/fp_peaks.json (python -m ...peaks);
+  FP32-accurate tensor rate: the tcgen05 TF32 rate / 3 (the 3xTF32 split), for the routes whose
+        contraction runs on the tensor cores; the f32 roof of such a route is max(FP32, TF32/3);
+  FP64  max(DFMA, DMMA) from the same file.
+The binding roof of a workload is the one whose time (bytes / bandwidth or flops / rate) is the
+larger; roof fraction = that time / measured time.
 
-Usage: python -m matrix_dense_linear_spd_gb300.report [--workloads f32_n8,...] [--reps 20]
-Prints one markdown table.
+Usage: python -m matrix_dense_linear_spd_gb300.report [--workloads f32_n8,...] [--steps 40]
+       [--saturation]   adds f32 n=8 at 2^20 items and the f32 n=32 Lower batch-doubling curve
+Prints markdown tables.
 """
 from __future__ import annotations
 
@@ -29,9 +36,10 @@ if _ROOT not in sys.path:
 import synth  # noqa: E402
 
 import matrix_dense_linear_spd_gb300 as bl  # noqa: E402
+from matrix_dense_linear_spd_gb300 import protocol as P  # noqa: E402
 
 ESIZE = {"f32": 4, "f64": 8, "c64": 8, "c128": 16}
-SMS, FP32_LANES, FP64_LANES = 152, 128, 2
+TENSOR_ROUTES = (":tc=2",)        # routes whose contraction runs on tcgen05 with the 3xTF32 split
 
 
 def tri_sector_bytes(n, dtype, uplo):
@@ -44,116 +52,151 @@ def tri_sector_bytes(n, dtype, uplo):
 
 
 def flops(n, dtype, nrhs=0):
+    """LAPACK counts: potrf, plus the two triangular solves per right-hand side."""
     c = synth.is_complex(dtype)
     f = (4 * n ** 3 / 3 + 3 * n ** 2 + 5 * n / 3) if c else (n ** 3 / 3 + n ** 2 / 2 + n / 6)
-    return f + nrhs * ((8 * n * n - 2 * n) if c else (2 * n * n - n)) * 2 / 2
+    return f + nrhs * ((8 * n * n - 2 * n) if c else (2 * n * n - n))
 
 
-def peaks(sm_mhz):
-    path = os.path.join(_ROOT, "MEASURED_PEAKS.json")
-    hbm = json.load(open(path))["hbm_gbs"] if os.path.exists(path) else 6800.0
-    f32 = SMS * FP32_LANES * 2 * sm_mhz * 1e6 / 1e12
-    f64 = SMS * FP64_LANES * 2 * sm_mhz * 1e6 / 1e12
-    return hbm, f32, f64
+def roofs():
+    """(HBM GB/s, FP32 TF/s, FP32-accurate tensor TF/s, FP64 TF/s, sources)."""
+    hp = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    fp = os.path.join(_ROOT, "profiles", "fp_peaks.json")
+    hbm = json.load(open(hp))["hbm_gbs"] if os.path.exists(hp) else 6800.0
+    src = ["HBM: " + ("MEASURED_PEAKS.json copy bandwidth" if os.path.exists(hp) else "fallback 6800 GB/s")]
+    if not os.path.exists(fp):
+        raise SystemExit("profiles/fp_peaks.json is missing: run python -m matrix_dense_linear_spd_gb300.peaks")
+    d = json.load(open(fp))["derived_tflops"]
+    src.append("FP: profiles/fp_peaks.json")
+    return hbm, d["fp32"], d["tf32x3"], d["fp64"], src
+
+
+def measure(w, op, uplo, nrhs, steps, torch, flush, l2, vendor, route=None):
+    n, batch, dt = w.n, w.batch, w.dtype
+    code = bl.DTYPE_CODES[dt]
+    s = torch.cuda.current_stream()
+    sp = s.cuda_stream
+    pa = torch.from_numpy(synth.to_colmajor(w.A)).cuda()
+    bufs = [pa]
+    if nrhs:
+        bufs.append(torch.from_numpy(synth.to_colmajor(w.B[:, :, :nrhs])).cuda())
+    total_bytes = sum(b.numel() * b.element_size() for b in bufs)
+    R = P.copies_per_chunk(total_bytes, l2, steps)
+    rot = P.Rotation(bufs, R)
+    infos = torch.zeros((R, batch), dtype=torch.int32, device="cuda")
+    if route:
+        bl.set_route(op, route)
+
+    def call(i):
+        if op == "potrf":
+            bl.potrf_ptr(uplo, code, n, batch, rot.ptr(0, i), n, n * n, infos[i].data_ptr(), sp)
+        else:
+            bl.posv_ptr(uplo, code, n, nrhs, batch, rot.ptr(0, i), n, n * n, rot.ptr(1, i), n, n * nrhs,
+                        infos[i].data_ptr(), sp)
+
+    try:
+        vcall = None
+        if vendor is not None and op == "potrf":
+            ptrs = [vendor.pointer_array(rot.ptr(0, i), batch, n * n, dt, pa.device) for i in range(R)]
+            vcall = lambda i: vendor.potrf(uplo, dt, n, batch, ptrs[i], n, infos[i].data_ptr(), sp)
+        ours, theirs = [], []
+        P.time_back_to_back(call, rot, flush, R, s)                 # warm-up chunk
+        if vcall:
+            P.time_back_to_back(vcall, rot, flush, R, s)
+        for rep in range(max(1, steps // R)):
+            order = [(call, ours), (vcall, theirs)] if rep % 2 == 0 else [(vcall, theirs), (call, ours)]
+            for fn, acc in order:
+                if fn is None:
+                    continue
+                pc, _ = P.time_back_to_back(fn, rot, flush, R, s, warm_chunks=0)
+                acc.extend(pc)
+        # correctness of the library's last chunk: info as planted (or all zero)
+        rot.restore()
+        call(0)
+        torch.cuda.synchronize()
+        expect = w.planted_info if w.planted_info is not None else np.zeros(batch, np.int32)
+        ok = np.array_equal(infos[0].cpu().numpy(), expect)
+        chosen = bl.last_choice()
+        iso = P.time_isolated(call, rot, flush, 15, s)
+    finally:
+        if route:
+            bl.set_route(op, None)
+    return {"ms": P.stats(ours)["median"], "rel_sd": P.stats(ours)["rel_sd"], "iso": P.stats(iso)["median"],
+            "vms": P.stats(theirs)["median"] if theirs else None, "route": chosen, "info_ok": ok}
+
+
+def row(name, w, op, uplo, nrhs, m, hbm, fp32, tf32x3, fp64):
+    n, batch, dt = w.n, w.batch, w.dtype
+    byts = (2 * tri_sector_bytes(n, dt, uplo) + 4) * batch
+    if nrhs:
+        byts += 2 * n * nrhs * ESIZE[dt] * batch
+    fl = flops(n, dt, nrhs) * batch
+    if dt in ("f64", "c128"):
+        fp, fpname = fp64, "FP64"
+    elif any(t in m["route"] for t in TENSOR_ROUTES):
+        fp, fpname = max(fp32, tf32x3), ("FP32" if fp32 >= tf32x3 else "3xTF32")
+    else:
+        fp, fpname = fp32, "FP32"
+    t_hbm, t_fp = byts / (hbm * 1e9), fl / (fp * 1e12)
+    bind = "HBM" if t_hbm >= t_fp else fpname
+    ms = m["ms"]
+    frac = max(t_hbm, t_fp) / (ms / 1e3)
+    vend = f"{m['vms']:.4f}" if m["vms"] else "-"
+    ratio = f"{m['vms'] / ms:.1f}" if m["vms"] else "-"
+    flag = "" if m["info_ok"] else " (info MISMATCH)"
+    noisy = " (noisy)" if m["rel_sd"] > 0.10 else ""
+    return (f"| {name} b{batch} | {op}{'' if not nrhs else f' nrhs={nrhs}'} | {uplo} | `{m['route']}` | "
+            f"{ms:.4f}{flag}{noisy} | {m['iso']:.4f} | {batch / (ms / 1e3):.3g} | {byts / (ms / 1e3) / 1e9:.0f} | "
+            f"{fl / (ms / 1e3) / 1e9:.0f} | {bind} | {frac:.2f} | {vend} | {ratio} |")
+
+
+HEADER = ("| workload | op | uplo | route | ms/call (back to back) | ms (isolated call) | matrices/s | "
+          "GB/s (triangle) | GFLOP/s | binding roof | roof frac | cuSOLVER ms | x vs cuSOLVER |\n"
+          "|---|---|---|---|---|---|---|---|---|---|---|---|---|")
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--workloads", default=",".join(synth.WORKLOADS))
-    ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--no-vendor", action="store_true")
+    ap.add_argument("--saturation", action="store_true")
+    ap.add_argument("--route", default=None, help="pin one route for every row (default: table choice)")
     a = ap.parse_args(argv)
     import torch
     dev = torch.cuda.get_device_properties(0)
     l2 = dev.L2_cache_size
-    fa = torch.empty(max(2 * l2, 256 << 20) // 4, device="cuda")
-    fb = torch.ones_like(fa)
-    sink = torch.empty((), device="cuda")
-    s = torch.cuda.current_stream()
-    hbm, f32p, f64p = peaks(2070.0)
-    print(f"| workload | op | uplo | route | ms/call | matrices/s | GB/s (triangle) | GFLOP/s | binding roof | "
-          f"roof frac | cuSOLVER ms | x vs cuSOLVER |")
-    print("|---|---|---|---|---|---|---|---|---|---|---|---|")
-    for name in a.workloads.split(","):
+    flush = P.L2Flush(l2, "cuda")
+    hbm, fp32, tf32x3, fp64, src = roofs()
+    vendor = None
+    if not a.no_vendor:
+        from matrix_dense_linear_spd_gb300.vendor import CusolverPotrfBatched
+        vendor = CusolverPotrfBatched()
+    print(HEADER)
+    for name in [x for x in a.workloads.split(",") if x]:
         w = synth.workload(name)
-        n, batch, dt = w.n, w.batch, w.dtype
-        code = bl.DTYPE_CODES[dt]
-        pr = torch.from_numpy(synth.to_colmajor(w.A)).cuda()
-        wk = pr.clone()
-        info = torch.empty(batch, dtype=torch.int32, device="cuda")
         ops = [("potrf", u, 0) for u in w.uplos]
         if w.nrhs:
             ops.append(("posv", "L", w.nrhs))
         for op, uplo, nrhs in ops:
-            if nrhs:
-                Bp = torch.from_numpy(synth.to_colmajor(w.B)).cuda()
-                Bw = Bp.clone()
-
-            def call():
-                if op == "potrf":
-                    bl.potrf_ptr(uplo, code, n, batch, wk.data_ptr(), n, n * n, info.data_ptr(), s.cuda_stream)
-                else:
-                    bl.posv_ptr(uplo, code, n, nrhs, batch, wk.data_ptr(), n, n * n, Bw.data_ptr(), n, n * nrhs,
-                                info.data_ptr(), s.cuda_stream)
-
-            ts = []
-            for it in range(a.reps + 3):
-                wk.copy_(pr)
-                if nrhs:
-                    Bw.copy_(Bp)
-                fa.zero_()
-                torch.sum(fb, dim=0, out=sink)
-                e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
-                e0.record(s)
-                call()
-                e1.record(s)
-                torch.cuda.synchronize()
-                if it >= 3:
-                    ts.append(e0.elapsed_time(e1))
-            ts.sort()
-            k = len(ts) // 5
-            ms = statistics.mean(ts[k:len(ts) - k] or ts)
-            route = bl.last_choice()
-            expect = w.planted_info if w.planted_info is not None else np.zeros(batch, np.int32)
-            ok = np.array_equal(info.cpu().numpy(), expect)
-            byts = (2 * tri_sector_bytes(n, dt, uplo) + 4) * batch
-            if nrhs:
-                byts += 2 * n * nrhs * ESIZE[dt] * batch
-            fl = flops(n, dt, nrhs) * batch
-            fp = f64p if dt in ("f64", "c128") else f32p
-            t_hbm = byts / (hbm * 1e9)
-            t_fp = fl / (fp * 1e12)
-            bind = "HBM" if t_hbm >= t_fp else ("FP64" if fp == f64p else "FP32")
-            frac = max(t_hbm, t_fp) / (ms / 1e3)
-            vend = "-"
-            ratio = "-"
-            if op == "potrf" and not a.no_vendor:
-                Av = wk.view(batch, n, n)
-                vt = []
-                for it in range(min(a.reps, 8) + 2):
-                    wk.copy_(pr)
-                    fa.zero_()
-                    torch.sum(fb, dim=0, out=sink)
-                    e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
-                    e0.record(s)
-                    torch.linalg.cholesky_ex(Av, upper=(uplo == "U"), check_errors=False)
-                    e1.record(s)
-                    torch.cuda.synchronize()
-                    if it >= 2:
-                        vt.append(e0.elapsed_time(e1))
-                vt.sort()
-                k = len(vt) // 5
-                vms = statistics.mean(vt[k:len(vt) - k] or vt)
-                vend = f"{vms:.4f}"
-                ratio = f"{vms / ms:.1f}"
-            flag = "" if ok else " (info MISMATCH)"
-            print(f"| {name} b{batch} | {op}{'' if not nrhs else f' nrhs={nrhs}'} | {uplo} | `{route}` | {ms:.4f}{flag} | "
-                  f"{batch / (ms / 1e3):.3g} | {byts / (ms / 1e3) / 1e9:.0f} | {fl / (ms / 1e3) / 1e9:.0f} | {bind} | "
-                  f"{frac:.2f} | {vend} | {ratio} |", flush=True)
-        del pr, wk
+            m = measure(w, op, uplo, nrhs, a.steps, torch, flush, l2, vendor, a.route)
+            print(row(name, w, op, uplo, nrhs, m, hbm, fp32, tf32x3, fp64), flush=True)
+        del w
         torch.cuda.empty_cache()
-    print(f"\nRoofs: HBM {hbm:.0f} GB/s (measured copy), FP32 {f32p:.1f} TFLOP/s and FP64 {f64p:.2f} TFLOP/s "
-          f"(unit counts at 2070 MHz).")
+    if a.saturation:
+        print("\nSaturation (potrf Lower, same protocol):\n")
+        print(HEADER)
+        cases = [("f32_n8", 1 << 20)] + [("f32_n32", 1 << k) for k in range(10, 18)]
+        for name, b in cases:
+            w = synth.workload(name, batch=b)
+            m = measure(w, "potrf", "L", 0, a.steps, torch, flush, l2, vendor)
+            print(row(name, w, "potrf", "L", 0, m, hbm, fp32, tf32x3, fp64), flush=True)
+            del w
+            torch.cuda.empty_cache()
+    print(f"\nRoofs: HBM {hbm:.0f} GB/s, FP32 {fp32:.1f} TFLOP/s, 3xTF32 {tf32x3:.1f} TFLOP/s (TF32 tensor / 3), "
+          f"FP64 {fp64:.2f} TFLOP/s; sources: {'; '.join(src)}.")
+    if vendor:
+        vendor.close()
     return 0
 
 
