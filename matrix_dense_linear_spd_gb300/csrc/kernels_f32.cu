@@ -21,8 +21,10 @@ static const KernelEntry k_entries_f32[] = {
     warp_entry<float, 16, 2>(),
     warp_entry<float, 16, 2, true>(),
     warp_entry<float, 16, 2, true, true>(),
+    warp_entry<float, 16, 2, true, true, true, true>(),
     warp_entry<float, 8, 4, true, true>(),
     warp_entry<float, 8, 2, true, true>(),
+    warp_entry<float, 8, 2, true, true, true, true>(),
     warp_entry<float, 32, 1>(),
     tile_entry<float, 2, 2>(),
     tile_entry<float, 2, 4>(),

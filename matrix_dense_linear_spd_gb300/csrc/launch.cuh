@@ -14,6 +14,7 @@
 #include "colblock_kernel.cuh"
 #include "tile_kernel.cuh"
 #include "warp_kernel.cuh"
+#include "warp2_kernel.cuh"
 #include "thread_kernel.cuh"
 
 namespace bl {
@@ -86,7 +87,7 @@ inline unsigned persistent_grid(K kern, int threads, size_t smem, int64_t ctas_n
 // compacted-triangle kernel like the plain variant (same arithmetic, bit-identical results).
 // PK: packed two-lane FP32 FMAs in the rank-1 update (f32), in both the factor-only and the
 // solve kernels.
-template <typename T, int P, int R, bool WHOLE = false, bool PK = false>
+template <typename T, int P, int R, bool WHOLE = false, bool PK = false, bool LA = false, bool V2 = false>
 cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     using C = WarpCfg<T, P, R>;
     const int64_t groups = (a.batch + C::G - 1) / C::G;
@@ -97,6 +98,17 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
                       a.stride_a == static_cast<int64_t>(C::N) * C::N && (reinterpret_cast<uintptr_t>(a.A) & 15) == 0;
     if (a.mode == MODE_POTRF) {
         if constexpr (WHOLE && C::full_ok) {
+            if constexpr (V2) {
+                if (full) {   // float2-pair rows (f32)
+                    auto kern = warp2_kernel<P, R, C::min_blocks_packed(), LA>;
+                    const size_t sm = a.upper ? C::smem_potrf_full : C::smem_full;
+                    static std::atomic<unsigned long long> done{0};
+                    cudaError_t e = ensure_smem(kern, C::smem_potrf_full, done);
+                    if (e != cudaSuccess) return e;
+                    kern<<<persistent_grid(kern, C::THREADS, sm, ctas), C::THREADS, sm, st>>>(a);
+                    return cudaGetLastError();
+                }
+            }
             if (full) {
                 auto kern = warp_kernel<T, P, R, false, PK ? C::min_blocks_packed() : C::min_blocks(), true, PK>;
                 const size_t sm = a.upper ? C::smem_potrf_full : C::smem_full;   // Upper stages its store
@@ -133,12 +145,16 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-template <typename T, int P, int R, bool WHOLE = false, bool PK = false>
+// V2: the whole-square factor-only kernel with float2 column-pair rows (warp2_kernel.cuh), LA
+// with look-ahead pivots; other calls of such a variant run the kernels of warp_kernel.cuh.
+template <typename T, int P, int R, bool WHOLE = false, bool PK = false, bool LA = false, bool V2 = false>
 constexpr KernelEntry warp_entry() {
     using C = WarpCfg<T, P, R>;
     static_assert(!WHOLE || C::full_ok, "whole-square slabs need whole 16-byte chunks per lane");
-    return KernelEntry{2, P, R, (WHOLE ? 1 : 0) | (PK ? 2 : 0), C::N, C::RHS, C::THREADS, C::PER_CTA,
-                       WHOLE ? C::smem_solve_full : C::smem_solve, &launch_warp<T, P, R, WHOLE, PK>};
+    static_assert(!V2 || (WHOLE && PK), "float2-pair rows: whole squares, packed update");
+    static_assert(!LA || V2, "look-ahead pivots: float2-pair rows");
+    return KernelEntry{2, P, R, (WHOLE ? 1 : 0) | (PK ? 2 : 0) | (LA ? 4 : 0) | (V2 ? 8 : 0), C::N, C::RHS, C::THREADS,
+                       C::PER_CTA, WHOLE ? C::smem_solve_full : C::smem_solve, &launch_warp<T, P, R, WHOLE, PK, LA, V2>};
 }
 
 template <typename T, int NMAX>

@@ -290,3 +290,29 @@ def test_upper_equals_lower_transposed_bitwise_for_real_types():
         U = synth.from_colmajor(ou, n, n, 4)
         low = np.tril(np.ones((n, n), bool))
         assert np.array_equal(L[:, low], np.swapaxes(U, -1, -2)[:, low]), n
+
+
+def test_look_ahead_and_pair_rows_are_bit_identical():
+    """The look-ahead variants (warp:...:la=1) form the next pivot on its owner lane with the
+    same fused multiply-add the rank-1 update applies, and the float2-pair-row variants
+    (warp:...:v2=1) apply the same operations in the same order as the packed variant: identical
+    bits and info to the plain packed variant, failures included."""
+    bl = lib()
+    rng = np.random.default_rng(23)
+    routes = {sp: cap for sp, cap, _ in bl.routes("f32")}
+    for sp, n in routes.items():
+        if ":la=1" not in sp and ":v2=1" not in sp:
+            continue
+        base = sp.replace(":la=1", "").replace(":v2=1", "")
+        assert base in routes, base
+        A = synth.spd_bbt(rng, n, 3001, "f32")
+        A[7, 0, 0] = -1.0
+        A[8, n - 1, n - 1] = -1.0
+        A[9, n // 2, n // 2] = np.nan
+        for uplo in "LU":
+            o0, i0, _ = _check_potrf(A, uplo, "f32", route=base)
+            o1, i1, _ = _check_potrf(A, uplo, "f32", route=sp)
+            assert np.array_equal(i0, i1)
+            f0, f1 = synth.from_colmajor(o0, n, n, 3001), synth.from_colmajor(o1, n, n, 3001)
+            ok = i0 == 0
+            assert np.array_equal(np.ascontiguousarray(f0[ok]).view(np.uint8), np.ascontiguousarray(f1[ok]).view(np.uint8)), sp
