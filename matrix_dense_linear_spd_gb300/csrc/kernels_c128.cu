@@ -11,10 +11,7 @@ static const KernelEntry k_entries_c128[] = {
     thread_entry<cf64, 18>(),
     warp_entry<cf64, 4, 2>(),
     warp_entry<cf64, 8, 1>(),
-    warp_entry<cf64, 8, 2>(),
     warp_entry<cf64, 16, 1>(),
-    warp_entry<cf64, 16, 2>(),
-    warp_entry<cf64, 32, 1>(),
     tile_entry<cf64, 2, 2>(),
     tile_entry<cf64, 2, 4>(),
     tile_entry<cf64, 4, 3>(),

@@ -110,7 +110,7 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
                 }
             }
             if (full) {
-                auto kern = warp_kernel<T, P, R, false, PK ? C::min_blocks_packed() : C::min_blocks(), true, PK>;
+                auto kern = warp_kernel<T, P, R, false, PK ? C::min_blocks_packed() : C::min_blocks_full(), true, PK>;
                 const size_t sm = a.upper ? C::smem_potrf_full : C::smem_full;   // Upper stages its store
                 static std::atomic<unsigned long long> done{0};
                 cudaError_t e = ensure_smem(kern, C::smem_potrf_full, done);

@@ -140,6 +140,12 @@ struct WarpCfg {
         const int m = 65536 / (THREADS * (row_words() + 45));
         return m < 1 ? 1 : (m > 8 ? 8 : m);
     }
+    // complex factor-only kernels on whole squares keep the 16-byte row reads of the pick live
+    // longer: one CTA per SM fewer than min_blocks() (ptxas spills otherwise)
+    static constexpr int min_blocks_full() {
+        const int m = min_blocks() - (is_cplx<T>::value ? 1 : 0);
+        return m < 1 ? 1 : m;
+    }
     // the packed update keeps column pairs in aligned register pairs: about 15 more per lane
     static constexpr int min_blocks_packed() {
         const int m = 65536 / (THREADS * (row_words() + 60));

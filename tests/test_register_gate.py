@@ -1,0 +1,74 @@
+"""Register gate (the "Batched Cholesky (potrf)" page's register-gate finding: a kernel that
+spills or keeps a stack frame is a defect to be caught at build time, and the gate itself must
+be able to fail). The build keeps ptxas's resource report of every translation unit; this test
+reads it and requires a zero stack frame and zero spill bytes for every kernel of the library,
+except the exceptions listed below with their exact figures (a listed kernel may not get worse,
+and an exception that no longer applies must be removed). A planted kernel with a dynamically
+indexed local array proves the gate fails when it should. Runs without a GPU."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+from matrix_dense_linear_spd_gb300 import build
+
+# mangled name -> (stack frame, spill stores, spill loads) that ptxas reports, and why it stays
+EXCEPTIONS = {
+    # the f32 column-block tensor-core kernel (Lower view): 255 registers, one 8-byte value spilled
+    "_ZN2bl15colblock_kernelIfLb0EEEvNS_9BatchArgsE": (8, 8, 8),
+}
+
+
+@pytest.fixture(scope="module")
+def reports():
+    build.build()
+    rep = build.ptxas_reports()
+    assert rep, "the build wrote no ptxas report"
+    return rep
+
+
+def test_every_kernel_is_free_of_stack_frames_and_spills(reports):
+    offenders, seen = [], set()
+    for tu, funcs in reports.items():
+        assert funcs, f"{tu}: empty ptxas report"
+        for f in funcs:
+            got = (f["stack"], f["spill_stores"], f["spill_loads"])
+            if f["name"] in EXCEPTIONS:
+                seen.add(f["name"])
+                lim = EXCEPTIONS[f["name"]]
+                assert all(g <= m for g, m in zip(got, lim)), f"{f['name']} got worse: {got} > {lim}"
+                assert got != (0, 0, 0), f"{f['name']} no longer spills: remove its exception"
+                continue
+            if got != (0, 0, 0):
+                offenders.append((tu, f["name"], got))
+    assert not offenders, f"stack frames or spills: {offenders}"
+    assert seen == set(EXCEPTIONS), f"exceptions for kernels that are not built: {set(EXCEPTIONS) - seen}"
+
+
+def test_register_counts_are_reported(reports):
+    kernels = [f for funcs in reports.values() for f in funcs if f["name"].startswith("_ZN2bl")]
+    assert len(kernels) > 50
+    assert all(f["registers"] is not None and 0 < f["registers"] <= 255 for f in kernels)
+
+
+PLANTED = r"""
+__global__ void planted(const int *idx, float *out) {
+    float a[64];
+    for (int i = 0; i < 64; ++i) a[(i * idx[0] + idx[1]) & 63] = out[i];   // run-time scatter and
+    out[threadIdx.x] = a[idx[threadIdx.x] & 63];                         // gather: a is on the stack
+}
+"""
+
+
+def test_the_gate_fails_on_a_planted_stack_frame(tmp_path):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    src = tmp_path / "planted.cu"
+    src.write_text(PLANTED)
+    r = subprocess.run([nvcc] + build.ARCH + ["-O3", "-Xptxas", "-v", "-c", str(src), "-o", str(tmp_path / "p.o")],
+                       capture_output=True, text=True, check=True)
+    funcs = build.parse_ptxas(r.stderr)
+    assert [f["name"] for f in funcs] == ["_Z7plantedPKiPf"]
+    assert funcs[0]["stack"] > 0                      # the gate's condition fires
