@@ -127,8 +127,18 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
         kern<<<persistent_grid(kern, C::THREADS, sm, ctas), C::THREADS, sm, st>>>(a);
     } else {
         if constexpr (WHOLE && C::full_solve_ok && C::smem_solve_full <= 227 * 1024) {
+            if constexpr (V2) {
+                if (full && a.mode == MODE_POSV) {   // float2-pair rows, fused solve (first pass)
+                    auto kern = warp2_kernel<P, R, C::min_blocks_solve(C::smem_solve_full), LA, true>;
+                    static std::atomic<unsigned long long> done{0};
+                    cudaError_t e = ensure_smem(kern, C::smem_solve_full, done);
+                    if (e != cudaSuccess) return e;
+                    kern<<<persistent_grid(kern, C::THREADS, C::smem_solve_full, ctas), C::THREADS, C::smem_solve_full, st>>>(a);
+                    return cudaGetLastError();
+                }
+            }
             if (full) {
-                auto kern = warp_kernel<T, P, R, true, 1, true, PK>;
+                auto kern = warp_kernel<T, P, R, true, C::min_blocks_solve(C::smem_solve_full), true, PK>;
                 static std::atomic<unsigned long long> done{0};
                 cudaError_t e = ensure_smem(kern, C::smem_solve_full, done);
                 if (e != cudaSuccess) return e;
@@ -136,7 +146,7 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
                 return cudaGetLastError();
             }
         }
-        auto kern = warp_kernel<T, P, R, true, 1, false, PK>;
+        auto kern = warp_kernel<T, P, R, true, C::min_blocks_solve(C::smem_solve), false, PK>;
         static std::atomic<unsigned long long> done{0};
         cudaError_t e = ensure_smem(kern, C::smem_solve, done);
         if (e != cudaSuccess) return e;
@@ -145,8 +155,9 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-// V2: the whole-square factor-only kernel with float2 column-pair rows (warp2_kernel.cuh), LA
-// with look-ahead pivots; other calls of such a variant run the kernels of warp_kernel.cuh.
+// V2: the whole-square kernel with float2 column-pair rows (warp2_kernel.cuh) for potrf and the
+// first pass of posv, LA with look-ahead pivots; other calls of such a variant (other layouts,
+// solve-only passes) run the kernels of warp_kernel.cuh.
 template <typename T, int P, int R, bool WHOLE = false, bool PK = false, bool LA = false, bool V2 = false>
 constexpr KernelEntry warp_entry() {
     using C = WarpCfg<T, P, R>;

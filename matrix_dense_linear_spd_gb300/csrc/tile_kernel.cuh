@@ -54,10 +54,8 @@ __device__ __forceinline__ void tile_sync() {
     if (WARP) __syncwarp(); else __syncthreads();
 }
 
-// The explicit minimum of one CTA per SM lets ptxas use the registers the tile needs; without it
-// ptxas caps the registers for occupancy and spills a few bytes (f32 16x6, 8x8, 8x6; c64 8x8, 8x6).
 template <typename T, int P, int S>
-__global__ void __launch_bounds__(TileCfg<T, P, S>::THREADS, 1)
+__global__ void __launch_bounds__(TileCfg<T, P, S>::THREADS)
 tile_kernel(const BatchArgs args) {
     using C = TileCfg<T, P, S>;
     using R = typename C::R;

@@ -37,11 +37,16 @@ __device__ __forceinline__ float &pel(float2 (&row)[NP], int c) {
     return (c & 1) ? row[c >> 1].y : row[c >> 1].x;
 }
 
-template <int P, int R, int MINB, bool LA>
+// SOLVE (posv, first pass): up to RHS right-hand sides per item ride along as in the lane-row
+// solve kernel: the forward substitution inside the column loop (y_j = b_j / L(j,j) published
+// next to the column, rows below subtract L(i,j) * y_j), the backward sweep after the factor
+// through a staging slab (the transpose of each block of P rows), the same operations in the
+// same order as warp_kernel.cuh's whole-square solve kernel.
+template <int P, int R, int MINB, bool LA, bool SOLVE = false>
 __global__ void __launch_bounds__(128, MINB) warp2_kernel(const BatchArgs args) {
     using C = WarpCfg<float, P, R>;
     constexpr int N = C::N, G = C::G, E = C::E, CB = C::CB, CBX = C::CBX, LDU = C::LDU;
-    constexpr int NP = N / 2;
+    constexpr int NP = N / 2, RHS = C::RHS, RB = C::RB;
     static_assert(N % 4 == 0 && P % 2 == 0, "column pairs and 16-byte column loads");
     extern __shared__ __align__(16) unsigned char smem[];
 
@@ -54,6 +59,9 @@ __global__ void __launch_bounds__(128, MINB) warp2_kernel(const BatchArgs args) 
     float *tri = reinterpret_cast<float *>(smem) + warp * G * C::FSTRIDE;
     float *colbuf = reinterpret_cast<float *>(smem + C::off_col_full) + slot * C::COLS;
     float *stage = reinterpret_cast<float *>(smem + C::off_stage + C::full_shift) + slot * P * LDU;
+    const int nrhs = SOLVE ? min(args.nrhs, RHS) : 0;
+    float *rsb = SOLVE ? reinterpret_cast<float *>(smem + C::off_rs + C::full_shift) + slot * N : nullptr;
+    float *xsb = SOLVE ? reinterpret_cast<float *>(smem + C::off_x + C::full_shift) + slot * 2 * RB : nullptr;
 
     const int64_t ngroups = (args.batch + G - 1) / G;
     const int64_t gstep = static_cast<int64_t>(gridDim.x) * C::WARPS;
@@ -95,7 +103,18 @@ __global__ void __launch_bounds__(128, MINB) warp2_kernel(const BatchArgs args) 
         __syncwarp();
         if (grp + gstep < ngroups) warp_prefetch<float, P, R, true>(args, tri, grp + gstep, lane, true);
 
-        // ---------------------------------------------------------- factor
+        // right-hand sides: b[r][c] = B(l + P*r, c)
+        float b[SOLVE ? R : 1][SOLVE ? RHS : 1];
+        float *Bm = SOLVE ? static_cast<float *>(args.B) + (live ? mat * args.stride_b : 0) : nullptr;
+        if (SOLVE) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int c = 0; c < RHS; ++c)
+                    b[r][c] = (live && c < nrhs) ? Bm[static_cast<int64_t>(c) * args.ldb + l + P * r] : 0.f;
+        }
+
+        // ---------------------------------------------------------- factor (+ forward solve)
         unsigned failed = 0;
         float dla = LA ? __shfl_sync(0xffffffffu, a[0][0].x, g * P) : 0.f;
 #pragma unroll
@@ -121,7 +140,33 @@ __global__ void __launch_bounds__(128, MINB) warp2_kernel(const BatchArgs args) 
                 const float t = fmaf(-pel(a[rj1], j), pel(a[rj1], j), pel(a[rj1], j + 1));
                 dla = __shfl_sync(0xffffffffu, t, g * P + lj1);
             }
+            if (SOLVE && l == lj) {
+                // forward substitution, axpy form: y_j = b_j / L(j,j), published next to the column
+#pragma unroll
+                for (int c = 0; c < RHS; ++c) {
+                    b[rj][c] = b[rj][c] * rs;
+                    col[CB + c] = b[rj][c];
+                }
+                rsb[j] = rs;
+            }
             __syncwarp();
+            if (SOLVE) {
+#pragma unroll
+                for (int q = 0; q < RB / E; ++q) {
+                    const float4 yv = reinterpret_cast<const float4 *>(col + CB)[q];
+                    const float ys[4] = {yv.x, yv.y, yv.z, yv.w};
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const int c = q * E + e;
+                        if (c >= RHS) continue;
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            if (P * r + P - 1 <= j) continue;      // no row > j in block r
+                            if (l + P * r > j) b[r][c] = fmaf(-pel(a[r], j), ys[e], b[r][c]);
+                        }
+                    }
+                }
+            }
             // rank-1 update of the trailing entries k > j, one packed FMA per column pair
 #pragma unroll
             for (int q = (j + 1) / 4; q < CB / 4; ++q) {
@@ -142,6 +187,54 @@ __global__ void __launch_bounds__(128, MINB) warp2_kernel(const BatchArgs args) 
             }
         }
         const int info = failed ? __ffs(failed) : 0;
+
+        // ---------------------------------------------------------- backward solve
+        if (SOLVE) {
+            // L^T x = y, one block of P rows at a time from the bottom: the block's rows of L are
+            // transposed through the staging slab, then x_i is broadcast and rows r < i subtract
+            // L(i,r) x_i
+#pragma unroll
+            for (int rb = R - 1; rb >= 0; --rb) {
+                __syncwarp();
+                {
+                    const int i = P * rb + l;
+#pragma unroll
+                    for (int k = 0; k < P * rb + P; ++k)
+                        if (k < i) stage[l * LDU + k] = pel(a[rb], k);
+                }
+                __syncwarp();
+                for (int ii = P - 1; ii >= 0; --ii) {
+                    const int i = P * rb + ii;
+                    float *xs = xsb + (i & 1) * RB;
+                    if (l == ii) {
+                        const float ri = rsb[i];
+#pragma unroll
+                        for (int c = 0; c < RHS; ++c) {
+                            b[rb][c] = b[rb][c] * ri;
+                            xs[c] = b[rb][c];
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int r = 0; r <= rb; ++r) {
+                        const int rr = l + P * r;
+                        if (rr < i) {
+                            const float lir = stage[ii * LDU + rr];
+#pragma unroll
+                            for (int c = 0; c < RHS; ++c) b[r][c] = fmaf(-lir, xs[c], b[r][c]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (info == 0 && live) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int c = 0; c < RHS; ++c)
+                        if (c < nrhs) Bm[static_cast<int64_t>(c) * args.ldb + l + P * r] = b[r][c];
+            }
+        }
 
         // ---------------------------------------------------------- store
         asm volatile("" : "+r"(l));

@@ -146,6 +146,15 @@ struct WarpCfg {
         const int m = min_blocks() - (is_cplx<T>::value ? 1 : 0);
         return m < 1 ? 1 : m;
     }
+    // solve kernels: the rows, the right-hand-side registers (R x RHS words per lane) and about 70
+    // for addresses, the broadcast solution values and temporaries (ptxas: no spill at this
+    // bound for the f32 geometries; the shared-memory footprint may still cap residency lower)
+    static constexpr int min_blocks_solve(size_t smem) {
+        const int m = 65536 / (THREADS * (row_words() + R * RHS * static_cast<int>(sizeof(T) / 4) + 70));
+        const int by_smem = static_cast<int>(233472 / (smem + 1024));    // 228 KB per SM, 1 KB per CTA reserved
+        const int b = m < by_smem ? m : by_smem;
+        return b < 1 ? 1 : (b > 8 ? 8 : b);
+    }
     // the packed update keeps column pairs in aligned register pairs: about 15 more per lane
     static constexpr int min_blocks_packed() {
         const int m = 65536 / (THREADS * (row_words() + 60));

@@ -86,28 +86,38 @@ def ledger_to_tables(records):
     return out
 
 
-def format_table(op, devkey, rows, source, date=None):
+def format_table(op, devkey, rows, source, date=None, top=12):
     keys = "dtype:exact uplo:exact n:log:3" + (" nrhs:log" if op != "potrf" else "") + " batch:log"
     lines = [f"# op={op} device={devkey} source=ledger:{source} date={date or time.strftime('%Y-%m-%d')} "
-             f"(median ms per call over two interleaved passes, back-to-back protocol, whole batch)",
+             f"(median ms per call over two interleaved passes, back-to-back protocol, whole batch; "
+             f"the {top} fastest verified candidates per row)",
              f"# keys: {keys}"]
     for key, ranked in rows:
         head = f"dtype={key['dtype']} uplo={key['uplo']} n={key['n']}"
         if op != "potrf":
             head += f" nrhs={key['nrhs']}"
         head += f" batch={key['batch']}"
-        lines.append(head + " | " + " | ".join(f"{sp} {ms:.5f}" for sp, ms in ranked) + " # measured")
+        lines.append(head + " | " + " | ".join(f"{sp} {ms:.5f}" for sp, ms in ranked[:top]) + " # measured")
     return "\n".join(lines) + "\n"
 
 
+def read_ledger(path):
+    import gzip
+    opener = gzip.open if path.endswith(".gz") else open
+    with opener(path, "rt") as f:
+        return [json.loads(x) for x in f if x.strip()]
+
+
 def write_tables(ledger_path, out_dir, devkey=None):
-    recs = [json.loads(x) for x in open(ledger_path) if x.strip()]
+    recs = []
+    for p in ledger_path.split(","):
+        recs += read_ledger(p)
     devkey = devkey or (recs[0]["device"] if recs else "sm_103")
     written = []
     for op, rows in ledger_to_tables(recs).items():
         path = os.path.join(out_dir, f"{op}.{devkey}.txt")
         with open(path, "w") as f:
-            f.write(format_table(op, devkey, rows, os.path.basename(ledger_path)))
+            f.write(format_table(op, devkey, rows, ",".join(os.path.basename(p) for p in ledger_path.split(","))))
         written.append(path)
     return written
 
@@ -231,7 +241,10 @@ def main(argv=None):
     ap.add_argument("--mem-budget", type=float, default=1.0, help="GiB per copy of a cell's batch")
     ap.add_argument("--out", required=True)
     ap.add_argument("--max-seconds", type=float, default=1e9)
-    ap.add_argument("--tables-from", default=None, help="only regenerate tables from this ledger")
+    ap.add_argument("--tables-from", default=None, help="only regenerate tables from these ledgers (comma list)")
+    ap.add_argument("--cells", default=None,
+                    help="explicit cells instead of the grid: dtype:uplo:n:batch[:nrhs] separated by commas")
+    ap.add_argument("--min-n", type=int, default=0, help="skip grid points below this n")
     a = ap.parse_args(argv)
     os.makedirs(a.out, exist_ok=True)
     if a.tables_from:
@@ -283,6 +296,18 @@ def main(argv=None):
         torch.cuda.empty_cache()
         return best
 
+    if a.cells:
+        for spec in a.cells.split(","):
+            f = spec.split(":")
+            dtype, uplo, n, batch = f[0], f[1], int(f[2]), int(f[3])
+            nrhs = int(f[4]) if len(f) > 4 else 0
+            w = measure(dtype, uplo, n, batch, nrhs, [sp for sp, cap, rhs in bl.routes(dtype)])
+            print(f"{a.op} {dtype} {uplo} n={n} nrhs={nrhs} batch={batch}: {w} (cell)", flush=True)
+        ledger.close()
+        for p in write_tables(ledger_path, a.out, devkey):
+            print(p)
+        return 0
+
     for dtype in a.dtypes.split(","):
         cands_all = [sp for sp, cap, rhs in bl.routes(dtype)]
         for uplo in a.uplos.split(","):
@@ -290,7 +315,7 @@ def main(argv=None):
                 for nrhs in nrhss:
                     winners = []
                     for n in ns:
-                        if n * n * ESIZE[dtype] * batch > a.mem_budget * (1 << 30):
+                        if n < a.min_n or n * n * ESIZE[dtype] * batch > a.mem_budget * (1 << 30):
                             continue
                         if time.time() - t_start > a.max_seconds:
                             break

@@ -316,3 +316,32 @@ def test_look_ahead_and_pair_rows_are_bit_identical():
             f0, f1 = synth.from_colmajor(o0, n, n, 3001), synth.from_colmajor(o1, n, n, 3001)
             ok = i0 == 0
             assert np.array_equal(np.ascontiguousarray(f0[ok]).view(np.uint8), np.ascontiguousarray(f1[ok]).view(np.uint8)), sp
+
+
+def test_pair_row_solve_is_bit_identical():
+    """posv on the float2-pair-row variants (fused solve, look-ahead pivots) gives the same bits
+    in A and B and the same info as the packed whole-square solve kernel, also when the
+    right-hand sides need a second, solve-only pass."""
+    bl = lib()
+    rng = np.random.default_rng(29)
+    routes = {sp: cap for sp, cap, _ in bl.routes("f32")}
+    for sp, n in routes.items():
+        if ":v2=1" not in sp:
+            continue
+        base = sp.replace(":la=1", "").replace(":v2=1", "")
+        A = synth.spd_bbt(rng, n, 777, "f32")
+        A[5, n // 3, n // 3] = -1.0
+        for nrhs in (3, 11):
+            B = synth.rhs_uniform(rng, n, nrhs, 777, "f32")
+            for uplo in "LU":
+                abuf, a0, bbuf, b0, i0 = call_posv(A, B, uplo, "f32", route=base)
+                _, a1, _, b1, i1 = call_posv(A, B, uplo, "f32", route=sp)
+                _, x, rinfo = oracle.run(uplo, n, 777, abuf, n, n * n, nrhs, bbuf, n, n * nrhs, threads=THREADS)
+                assert np.array_equal(i1, rinfo) and np.array_equal(i0, i1)
+                ok = i1 == 0
+                X1 = synth.from_colmajor(b1, n, nrhs, 777)
+                assert solution_errors(X1[ok], x[ok]).max() <= TOL_X["f32"], sp
+                assert np.array_equal(b0.view(np.uint8), b1.view(np.uint8)), (sp, nrhs, uplo)
+                f0, f1 = synth.from_colmajor(a0, n, n, 777), synth.from_colmajor(a1, n, n, 777)
+                assert np.array_equal(np.ascontiguousarray(f0[ok]).view(np.uint8),
+                                      np.ascontiguousarray(f1[ok]).view(np.uint8)), (sp, nrhs, uplo)

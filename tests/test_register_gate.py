@@ -17,6 +17,15 @@ from matrix_dense_linear_spd_gb300 import build
 EXCEPTIONS = {
     # the f32 column-block tensor-core kernel (Lower view): 255 registers, one 8-byte value spilled
     "_ZN2bl15colblock_kernelIfLb0EEEvNS_9BatchArgsE": (8, 8, 8),
+    # register-tile kernels: ptxas caps their registers for occupancy and spills one to six words;
+    # a minimum of one CTA per SM removes the spill but raises the registers and halves the
+    # occupancy of the larger tiles (c64 n=128 on tile:p=16:s=8: 1.96 -> 3.19 ms), so they keep
+    # the cap
+    "_ZN2bl11tile_kernelIfLi16ELi6EEEvNS_9BatchArgsE": (8, 4, 4),
+    "_ZN2bl11tile_kernelIfLi8ELi8EEEvNS_9BatchArgsE": (8, 8, 8),
+    "_ZN2bl11tile_kernelIfLi8ELi6EEEvNS_9BatchArgsE": (16, 12, 12),
+    "_ZN2bl11tile_kernelINS_4cf32ELi8ELi8EEEvNS_9BatchArgsE": (16, 24, 24),
+    "_ZN2bl11tile_kernelINS_4cf32ELi8ELi6EEEvNS_9BatchArgsE": (8, 4, 4),
 }
 
 
