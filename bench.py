@@ -138,30 +138,36 @@ def host_cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
-def cpu_oracle_rate(w, uplo: str, target_s: float = 8.0, max_items: int = 4096, reps: int = 3):
-    """Oracle matrices/s on the host cores over a bounded leading sample of the workload:
-    the sample is sized by one calibration run to about target_s / reps of wall time, then
-    timed `reps` times; the median is reported."""
+def cpu_oracle_rate(w, uplo: str, target_s: float = 10.0, max_items: int | None = None, reps: int = 3):
+    """Oracle matrices/s on the host cores over a bounded sample of the workload: the leading
+    items, grown until one run takes about target_s / reps (at most the whole batch); then the
+    sample is run repeatedly, at least `reps` times and until about target_s of CPU work is done,
+    and the median run is reported. Returns (rate, items per run, median s, cores, long-double
+    mantissa bits, runs)."""
     import oracle
     cores = os.cpu_count() or 1
     n = w.n
-    k = min(max(cores, 64), w.batch)
+    cap = w.batch if max_items is None else min(max_items, w.batch)
+    k = min(max(cores, 64), cap)
     per_run = target_s / max(reps, 1)
     while True:
         buf = synth.to_colmajor(w.A[:k])
         t0 = time.perf_counter()
         oracle.run(uplo, n, k, buf, n, n * n, threads=cores)
         t = time.perf_counter() - t0
-        if t >= per_run or k >= min(max_items, w.batch):
+        if t >= per_run or k >= cap:
             break
-        k = min(min(max_items, w.batch), max(k * 2, int(k * per_run / max(t, 1e-3))))
-    ts = []
-    for _ in range(reps):
+        k = min(cap, max(k * 2, int(k * per_run / max(t, 1e-3))))
+    ts, total = [], 0.0
+    while len(ts) < reps or total < target_s:
         t0 = time.perf_counter()
         oracle.run(uplo, n, k, buf, n, n * n, threads=cores)
         ts.append(time.perf_counter() - t0)
+        total += ts[-1]
+        if len(ts) >= 1000:
+            break
     t = statistics.median(ts)
-    return k / t, k, t, cores, oracle.long_double_digits()
+    return k / t, k, t, cores, oracle.long_double_digits(), len(ts)
 
 
 # ------------------------------------------------------------------ the GPU arm
@@ -353,9 +359,11 @@ def run_ours(args, ws, rank, local):
         "also": also,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rate, k, t, cores, ldig = cpu_oracle_rate(w, "L", target_s=args.cpu_seconds)
+        rate, k, t, cores, ldig, runs = cpu_oracle_rate(w, "L", target_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"first {k} items of the workload, median of 3 runs ({t:.2f} s each)",
+                                "sample": (f"{'the whole batch' if k == w.batch else f'the first {k} items'} "
+                                           f"({k} matrices) per run, {runs} runs (~{runs * t:.0f} s of CPU "
+                                           f"work), median run {t:.3f} s"),
                                 "cpu": host_cpu_model(),
                                 "long_double": {64: "x87 80-bit extended", 113: "IEEE binary128 (software)"}.get(
                                     ldig, f"{ldig}-bit mantissa")}
@@ -369,7 +377,7 @@ def run_reference(args):
     import oracle
     w = synth.workload(args.workload)
     cores = os.cpu_count() or 1
-    rate0, k, t, _, ldig = cpu_oracle_rate(w, "L", target_s=min(args.cpu_seconds, 3.0), max_items=2048, reps=1)
+    rate0, k, t, _, ldig, _ = cpu_oracle_rate(w, "L", target_s=min(args.cpu_seconds, 3.0), max_items=2048, reps=1)
     per_step = max(1, min(w.batch, int(rate0 * args.reference_step_seconds)))
     buf = synth.to_colmajor(w.A[:per_step])
     for _ in range(args.warmup):
@@ -404,7 +412,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="f32_n32", choices=list(synth.WORKLOADS))
     ap.add_argument("--warm-seconds", type=float, default=1.0)
-    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-step-seconds", type=float, default=0.5)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

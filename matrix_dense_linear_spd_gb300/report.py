@@ -122,7 +122,8 @@ def measure(w, op, uplo, nrhs, steps, torch, flush, l2, vendor, route=None):
         if route:
             bl.set_route(op, None)
     return {"ms": P.stats(ours)["median"], "rel_sd": P.stats(ours)["rel_sd"], "iso": P.stats(iso)["median"],
-            "vms": P.stats(theirs)["median"] if theirs else None, "route": chosen, "info_ok": ok}
+            "vms": P.stats(theirs)["median"] if theirs else None, "route": chosen, "info_ok": ok,
+            "l2_resident": R * total_bytes < 4 * l2}
 
 
 def row(name, w, op, uplo, nrhs, m, hbm, fp32, tf32x3, fp64):
@@ -145,6 +146,8 @@ def row(name, w, op, uplo, nrhs, m, hbm, fp32, tf32x3, fp64):
     ratio = f"{m['vms'] / ms:.1f}" if m["vms"] else "-"
     flag = "" if m["info_ok"] else " (info MISMATCH)"
     noisy = " (noisy)" if m["rel_sd"] > 0.10 else ""
+    if m.get("l2_resident"):
+        noisy += " (a chunk's copies fit in L2)"
     return (f"| {name} b{batch} | {op}{'' if not nrhs else f' nrhs={nrhs}'} | {uplo} | `{m['route']}` | "
             f"{ms:.4f}{flag}{noisy} | {m['iso']:.4f} | {batch / (ms / 1e3):.3g} | {byts / (ms / 1e3) / 1e9:.0f} | "
             f"{fl / (ms / 1e3) / 1e9:.0f} | {bind} | {frac:.2f} | {vend} | {ratio} |")
