@@ -23,6 +23,7 @@ static const KernelEntry k_entries_f32[] = {
     warp_entry<float, 16, 2, true, true>(),
     warp_entry<float, 16, 2, true, true, true, true>(),
     warp_entry<float, 8, 4, true, true>(),
+    warp_entry<float, 8, 4, true, true, true, true>(),
     warp_entry<float, 8, 2, true, true>(),
     warp_entry<float, 8, 2, true, true, true, true>(),
     warp_entry<float, 32, 1>(),

@@ -99,11 +99,13 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
     if (a.mode == MODE_POTRF) {
         if constexpr (WHOLE && C::full_ok) {
             if constexpr (V2) {
-                if (full) {   // float2-pair rows (f32)
-                    auto kern = warp2_kernel<P, R, C::min_blocks_packed(), LA>;
-                    const size_t sm = a.upper ? C::smem_potrf_full : C::smem_full;
+                if (full) {   // float2-pair rows (f32); Upper stages its store
+                    constexpr bool cs = C::v2_compact;
+                    auto kern = warp2_kernel<P, R, cs ? C::min_blocks_v2c() : C::min_blocks_packed(), LA, false, cs>;
+                    constexpr size_t sm_up = cs ? C::smem_potrf : C::smem_potrf_full;
+                    const size_t sm = a.upper ? sm_up : (cs ? C::smem_lower : C::smem_full);
                     static std::atomic<unsigned long long> done{0};
-                    cudaError_t e = ensure_smem(kern, C::smem_potrf_full, done);
+                    cudaError_t e = ensure_smem(kern, sm_up, done);
                     if (e != cudaSuccess) return e;
                     kern<<<persistent_grid(kern, C::THREADS, sm, ctas), C::THREADS, sm, st>>>(a);
                     return cudaGetLastError();
@@ -129,11 +131,13 @@ cudaError_t launch_warp(const BatchArgs &a, cudaStream_t st) {
         if constexpr (WHOLE && C::full_solve_ok && C::smem_solve_full <= 227 * 1024) {
             if constexpr (V2) {
                 if (full && a.mode == MODE_POSV) {   // float2-pair rows, fused solve (first pass)
-                    auto kern = warp2_kernel<P, R, C::min_blocks_solve(C::smem_solve_full), LA, true>;
+                    constexpr bool cs = C::v2_compact;
+                    constexpr size_t sm = cs ? C::smem_solve : C::smem_solve_full;
+                    auto kern = warp2_kernel<P, R, C::min_blocks_solve(sm), LA, true, cs>;
                     static std::atomic<unsigned long long> done{0};
-                    cudaError_t e = ensure_smem(kern, C::smem_solve_full, done);
+                    cudaError_t e = ensure_smem(kern, sm, done);
                     if (e != cudaSuccess) return e;
-                    kern<<<persistent_grid(kern, C::THREADS, C::smem_solve_full, ctas), C::THREADS, C::smem_solve_full, st>>>(a);
+                    kern<<<persistent_grid(kern, C::THREADS, sm, ctas), C::THREADS, sm, st>>>(a);
                     return cudaGetLastError();
                 }
             }

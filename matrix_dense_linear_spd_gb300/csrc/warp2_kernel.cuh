@@ -17,6 +17,11 @@
 // !(d > 0) fails (first failure wins, info = j+1), L(j,j) = d * rsqrt(d), L(i,j) = A(i,j) *
 // rsqrt(d), A(i,k) -= L(i,j) * L(k,j) for j < k <= i.
 //
+// Slabs: whole squares (stride FSTRIDE, the copy moves only the chunks that meet the triangle) or,
+// with CSLAB, compacted triangles (TriSlab, about 56% of the square at n = 32), for geometries
+// whose whole-square slabs would hold fewer CTAs per SM than the registers allow.
+
+//
 // Look-ahead pivots (LA): the lane that owns row j+1 forms the next pivot,
 // A(j+1,j+1) - L(j+1,j)^2, from its own registers right after column j is scaled and shuffles
 // it at once, so the pivot chain (shuffle, rsqrt, scale, one FMA, shuffle) no longer waits for
@@ -37,16 +42,58 @@ __device__ __forceinline__ float &pel(float2 (&row)[NP], int c) {
     return (c & 1) ? row[c >> 1].y : row[c >> 1].x;
 }
 
+// Copy one group's contiguous run of whole squares (lda = N, item stride N*N) into compacted
+// slabs (TriSlab layout, matrix stride MS). Lane (gg, q) = (lane / (N/E), lane mod (N/E)) owns
+// chunk q (rows q*E .. q*E+E-1) of matrix gg and sweeps the columns: source and slab offsets are
+// lane-fixed bases plus compile-time constants, and the chunk moves for the columns where it
+// meets the referenced triangle (Lower: c < q*E + E; Upper: c >= q*E).
+template <bool UPPER, int N, int E, int MS, int G>
+__device__ __forceinline__ void compact_copy(float *tri, const float *A0, int lane, int64_t mleft) {
+    constexpr int NQ = N / E;
+    static_assert(G * NQ == 32, "one lane per (matrix, chunk)");
+    using L = TriSlab<N, E>;
+    const int gg = lane / NQ, q = lane - gg * NQ;
+    if (gg >= mleft) return;
+    const float *src = A0 + gg * (N * N) + q * E;
+    float *dst = tri + gg * MS + q * E;
+#pragma unroll
+    for (int t = 0; t < NQ; ++t) {                 // columns E*t .. E*t+E-1 share the test
+        if (UPPER ? (q > t) : (q < t)) continue;
+#pragma unroll
+        for (int c = E * t; c < E * t + E; ++c)
+            cp_async_16(dst + (UPPER ? L::up_off(c) : L::lo_off(c) - L::lo_first(c)), src + c * N);
+    }
+}
+
+// Prefetch group `grp` (whole squares, back to back) into the warp's slab: whole-square slabs
+// (stride FSTRIDE) or, with CSLAB, compacted ones (stride MSTRIDE).
+template <int P, int R, bool CSLAB>
+__device__ __forceinline__ void warp2_prefetch(const BatchArgs &args, float *tri, int64_t grp, int lane) {
+    using C = WarpCfg<float, P, R>;
+    if constexpr (CSLAB) {
+        const float *A0 = static_cast<const float *>(args.A) + grp * C::G * static_cast<int64_t>(C::N * C::N);
+        const int64_t mleft = args.batch - grp * C::G;
+        if (args.upper) compact_copy<true, C::N, C::E, C::MSTRIDE, C::G>(tri, A0, lane, mleft);
+        else compact_copy<false, C::N, C::E, C::MSTRIDE, C::G>(tri, A0, lane, mleft);
+        cp_async_commit();
+    } else {
+        warp_prefetch<float, P, R, true>(args, tri, grp, lane, true);
+    }
+}
+
 // SOLVE (posv, first pass): up to RHS right-hand sides per item ride along as in the lane-row
 // solve kernel: the forward substitution inside the column loop (y_j = b_j / L(j,j) published
 // next to the column, rows below subtract L(i,j) * y_j), the backward sweep after the factor
 // through a staging slab (the transpose of each block of P rows), the same operations in the
 // same order as warp_kernel.cuh's whole-square solve kernel.
-template <int P, int R, int MINB, bool LA, bool SOLVE = false>
+template <int P, int R, int MINB, bool LA, bool SOLVE = false, bool CSLAB = false>
 __global__ void __launch_bounds__(128, MINB) warp2_kernel(const BatchArgs args) {
     using C = WarpCfg<float, P, R>;
+    using L = TriSlab<C::N, C::E>;
     constexpr int N = C::N, G = C::G, E = C::E, CB = C::CB, CBX = C::CBX, LDU = C::LDU;
     constexpr int NP = N / 2, RHS = C::RHS, RB = C::RB;
+    constexpr int SLAB = CSLAB ? C::MSTRIDE : C::FSTRIDE;          // per-matrix slab stride
+    constexpr size_t SHIFT = CSLAB ? 0 : C::full_shift;             // where the other areas start
     static_assert(N % 4 == 0 && P % 2 == 0, "column pairs and 16-byte column loads");
     extern __shared__ __align__(16) unsigned char smem[];
 
@@ -56,17 +103,17 @@ __global__ void __launch_bounds__(128, MINB) warp2_kernel(const BatchArgs args) 
     const int l_in = lane - g * P;
     const int slot = warp * G + g;
     const bool upper = args.upper != 0;
-    float *tri = reinterpret_cast<float *>(smem) + warp * G * C::FSTRIDE;
-    float *colbuf = reinterpret_cast<float *>(smem + C::off_col_full) + slot * C::COLS;
-    float *stage = reinterpret_cast<float *>(smem + C::off_stage + C::full_shift) + slot * P * LDU;
+    float *tri = reinterpret_cast<float *>(smem) + warp * G * SLAB;
+    float *colbuf = reinterpret_cast<float *>(smem + C::off_col + SHIFT) + slot * C::COLS;
+    float *stage = reinterpret_cast<float *>(smem + C::off_stage + SHIFT) + slot * P * LDU;
     const int nrhs = SOLVE ? min(args.nrhs, RHS) : 0;
-    float *rsb = SOLVE ? reinterpret_cast<float *>(smem + C::off_rs + C::full_shift) + slot * N : nullptr;
-    float *xsb = SOLVE ? reinterpret_cast<float *>(smem + C::off_x + C::full_shift) + slot * 2 * RB : nullptr;
+    float *rsb = SOLVE ? reinterpret_cast<float *>(smem + C::off_rs + SHIFT) + slot * N : nullptr;
+    float *xsb = SOLVE ? reinterpret_cast<float *>(smem + C::off_x + SHIFT) + slot * 2 * RB : nullptr;
 
     const int64_t ngroups = (args.batch + G - 1) / G;
     const int64_t gstep = static_cast<int64_t>(gridDim.x) * C::WARPS;
     int64_t grp = static_cast<int64_t>(blockIdx.x) * C::WARPS + warp;
-    if (grp < ngroups) warp_prefetch<float, P, R, true>(args, tri, grp, lane, true);
+    if (grp < ngroups) warp2_prefetch<P, R, CSLAB>(args, tri, grp, lane);
 
     for (; grp < ngroups; grp += gstep) {
         int l = l_in;
@@ -78,20 +125,24 @@ __global__ void __launch_bounds__(128, MINB) warp2_kernel(const BatchArgs args) 
         float2 a[R][NP];
         cp_async_wait_all();
         __syncwarp();
-        const float *my = tri + g * C::FSTRIDE;
+        const float *my = tri + g * SLAB;
         if (!upper) {
 #pragma unroll
             for (int c = 0; c < N; ++c)
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (P * r + P - 1 < c) continue;          // block r has no row >= c
-                    pel(a[r], c) = my[c * C::NS_L + l + P * r];
+                    pel(a[r], c) = CSLAB ? my[L::lo_off(c) - L::lo_first(c) + l + P * r]
+                                         : my[c * C::NS_L + l + P * r];
                 }
         } else {
-            // row i of S is column i of A: 16 bytes (two pairs) at a time
+            // row i of S is column i of A: 16 bytes (two pairs) at a time; in a compacted slab
+            // the reads past column i's kept rows land in the next column (entries right of the
+            // diagonal of S, never read into the factor) and stay inside the matrix's slab
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const float4 *rowp = reinterpret_cast<const float4 *>(my + (l + P * r) * C::NS);
+                const float4 *rowp = reinterpret_cast<const float4 *>(
+                    my + (CSLAB ? upper_slab_offset(l + P * r, E) : (l + P * r) * C::NS));
 #pragma unroll
                 for (int c4 = 0; c4 < (P * r + P) / 4; ++c4) {
                     const float4 v = rowp[c4];
@@ -101,7 +152,7 @@ __global__ void __launch_bounds__(128, MINB) warp2_kernel(const BatchArgs args) 
             }
         }
         __syncwarp();
-        if (grp + gstep < ngroups) warp_prefetch<float, P, R, true>(args, tri, grp + gstep, lane, true);
+        if (grp + gstep < ngroups) warp2_prefetch<P, R, CSLAB>(args, tri, grp + gstep, lane);
 
         // right-hand sides: b[r][c] = B(l + P*r, c)
         float b[SOLVE ? R : 1][SOLVE ? RHS : 1];
@@ -255,7 +306,9 @@ __global__ void __launch_bounds__(128, MINB) warp2_kernel(const BatchArgs args) 
             }
         } else {
             // U(c,i) = L(i,c): column i of U is row i of L; transpose through the staging slab,
-            // one block of P rows (= P columns of U) at a time
+            // one block of P rows (= P columns of U) at a time; lanes write consecutive rows of a
+            // column of U, 32-bit coalesced stores (per-lane 16-byte pieces of a column of U,
+            // 32 lines per store instruction, measured slower: f32 n=32 Upper 28.9 us against 26.0)
 #pragma unroll
             for (int cb = 0; cb < R; ++cb) {
                 const int c0 = P * cb;

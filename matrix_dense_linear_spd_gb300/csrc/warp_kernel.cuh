@@ -160,6 +160,17 @@ struct WarpCfg {
         const int m = 65536 / (THREADS * (row_words() + 60));
         return m < 1 ? 1 : (m > 8 ? 8 : m);
     }
+    // float2-row kernels on compacted slabs: the rows are their own register pairs, about 48 more
+    // for addresses, the column pieces in flight and the pivot chain
+    static constexpr int min_blocks_v2c() {
+        const int m = 65536 / (THREADS * (row_words() + 48));
+        return m < 1 ? 1 : (m > 8 ? 8 : m);
+    }
+    static constexpr int blocks_by_smem(size_t bytes) { return static_cast<int>(233472 / (bytes + 1024)); }
+    // the float2-row kernel takes the compacted slab when whole-square slabs would hold fewer CTAs
+    // per SM than its registers allow and one sweep of 32 lanes spans E whole columns
+    static constexpr bool v2_compact = sizeof(T) == 4 && N / E > 0 && 32 % (N / E) == 0 && 32 / (N / E) == E &&
+                                       (N * N / E) % 32 == 0 && blocks_by_smem(smem_full) < min_blocks_v2c();
 };
 
 template <typename T>

@@ -276,6 +276,33 @@ def test_edge_cases_and_argument_errors():
     torch.cuda.synchronize()
 
 
+def test_pair_row_routes_leave_the_other_triangle():
+    """Every float2-pair-row route, pinned: NaN in the other triangle changes no bit of the
+    factor (its slab copy and pick read only the referenced triangle's values into the factor)
+    and a sentinel there survives (the Upper store writes column i of U only in rows <= i)."""
+    bl = lib()
+    rng = np.random.default_rng(31)
+    for sp, n, _ in bl.routes("f32"):
+        if ":v2=1" not in sp:
+            continue
+        A = synth.spd_bbt(rng, n, 37, "f32")
+        for uplo in "LU":
+            other = ~(np.tril(np.ones((n, n), bool)) if uplo == "L" else np.triu(np.ones((n, n), bool)))
+            P = A.copy()
+            P[:, other] = np.nan
+            S = A.copy()
+            S[:, other] = -999
+            _, o0, i0, _, _ = call_potrf(A, uplo, "f32", route=sp)
+            _, o1, i1, _, _ = call_potrf(P, uplo, "f32", route=sp)
+            in2, o2, i2, _, _ = call_potrf(S, uplo, "f32", route=sp)
+            tri = ~other
+            f0, f1 = synth.from_colmajor(o0, n, n, 37), synth.from_colmajor(o1, n, n, 37)
+            assert np.array_equal(np.ascontiguousarray(f0[:, tri]).view(np.uint8),
+                                  np.ascontiguousarray(f1[:, tri]).view(np.uint8)), (sp, uplo)
+            assert not i0.any() and not i1.any() and not i2.any(), (sp, uplo)
+            assert other_triangle_unchanged(in2, o2, n, 37, n, n * n, uplo), (sp, uplo)
+
+
 def test_upper_equals_lower_transposed_bitwise_for_real_types():
     """Upper is a load/store transform of the same recurrence: for real types the Upper factor
     is bit-identical to the transposed Lower factor."""

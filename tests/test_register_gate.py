@@ -26,6 +26,13 @@ EXCEPTIONS = {
     "_ZN2bl11tile_kernelIfLi8ELi6EEEvNS_9BatchArgsE": (16, 12, 12),
     "_ZN2bl11tile_kernelINS_4cf32ELi8ELi8EEEvNS_9BatchArgsE": (16, 24, 24),
     "_ZN2bl11tile_kernelINS_4cf32ELi8ELi6EEEvNS_9BatchArgsE": (8, 4, 4),
+    # float2-row kernel, 8 lanes x 4 rows (four matrices per warp, compacted slabs): 80 words of
+    # rows per lane; it spills at every bound tried (128, 168 and 255 registers; also with the
+    # prefetch or the Upper path compiled out), the least at these. The factor-only kernel loses
+    # to the 16 x 2 geometry (f32 n=32 b16384 Lower 29.4 us against 22.9) and stays a tuner
+    # candidate; the fused posv kernel is the fastest measured (nrhs=4 50.4 us against 57.6)
+    "_ZN2bl12warp2_kernelILi8ELi4ELi4ELb1ELb0ELb1EEEvNS_9BatchArgsE": (48, 80, 92),
+    "_ZN2bl12warp2_kernelILi8ELi4ELi3ELb1ELb1ELb1EEEvNS_9BatchArgsE": (64, 100, 96),
 }
 
 
