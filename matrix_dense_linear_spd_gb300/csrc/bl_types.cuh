@@ -116,6 +116,9 @@ __device__ __forceinline__ void cp_async_elem(void *dst, const void *src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+// wait until at most N of this thread's most recent commit groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 // Operation selector shared by the kernels.
 enum Mode : int { MODE_POTRF = 0, MODE_POSV = 1, MODE_POTRS = 2 };

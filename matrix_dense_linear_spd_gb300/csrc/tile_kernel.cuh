@@ -46,12 +46,44 @@ struct TileCfg {
     static constexpr size_t off_x = off_col + sizeof(T) * 2 * G * P * CS;
     static constexpr size_t off_rs = off_x + sizeof(T) * 2 * G * P;
     static constexpr size_t off_info = off_rs + sizeof(R) * G * N;
-    static constexpr size_t smem_bytes = ((off_info + sizeof(int) * G) + 15) / 16 * 16;
+    // second staging buffer: the load copies block b+1 while block b is distributed
+    static constexpr size_t off_stage1 = ((off_info + sizeof(int) * G) + 15) / 16 * 16;
+    static constexpr size_t smem_bytes = off_stage1 + sizeof(T) * G * P * LDST;
 };
 
 template <bool WARP>
 __device__ __forceinline__ void tile_sync() {
     if (WARP) __syncwarp(); else __syncthreads();
+}
+
+// Issue the copies of staging block b (P columns of A, or P rows of S = columns of A for Upper)
+// into buffer b & 1 as element-wise cp.async, and close one commit group (empty past the
+// matrix). RT threads walk a column, CT columns at a time; thread (sr, sc) of the matrix.
+template <typename T, int P, int RT, int CT, int LDST>
+__device__ __forceinline__ void tile_issue(int b, bool live, bool upper, int n, int64_t lda, const T *A, T *stage0,
+                                           T *stage1, int sr, int sc) {
+    const int c0 = b * P;
+    T *buf = (b & 1) ? stage1 : stage0;
+    if (live && c0 < n) {
+        if (!upper) {
+            // columns c0..c0+P-1 of A, rows c..n-1 (lower part only)
+            for (int cc = sc; cc < P; cc += CT) {
+                const int c = c0 + cc;
+                if (c >= n) break;
+                for (int r = c + sr; r < n; r += RT)
+                    cp_async_elem<sizeof(T)>(buf + cc * LDST + r, A + static_cast<int64_t>(c) * lda + r);
+            }
+        } else {
+            // rows c0..c0+P-1 of S = columns of A, A rows 0..i (upper part only)
+            for (int ii = sc; ii < P; ii += CT) {
+                const int i = c0 + ii;
+                if (i >= n) break;
+                for (int k = sr; k <= i; k += RT)
+                    cp_async_elem<sizeof(T)>(buf + ii * LDST + k, A + static_cast<int64_t>(i) * lda + k);
+            }
+        }
+    }
+    cp_async_commit();
 }
 
 template <typename T, int P, int S>
@@ -103,43 +135,40 @@ tile_kernel(const BatchArgs args) {
     if (tl == 0) info_all[g] = 0;
 
     // ------------------------------------------------------------------ load A (staged)
+    // Block b (P columns of A, or P rows of S for Upper) moves by element-wise cp.async into one
+    // of two staging buffers, every copy of the block in flight at once and no register round
+    // trip; block b+1 is issued before block b is distributed into the tile, so its HBM latency
+    // overlaps that work. One commit group per block (empty past the matrix), waited for with
+    // one group still in flight.
+    T *const stage1 = reinterpret_cast<T *>(smem + C::off_stage1) + g * P * LDST;
+    const bool do_load = live;
+    tile_issue<T, P, RT, CT, LDST>(0, do_load, upper, n, lda, A, stage, stage1, sr, sc);
 #pragma unroll
     for (int b = 0; b < S; ++b) {
         const int c0 = b * P;
         if (c0 >= n) break;
+        tile_issue<T, P, RT, CT, LDST>(b + 1, do_load, upper, n, lda, A, stage, stage1, sr, sc);
+        cp_async_wait_group<1>();
+        tile_sync<WS>();
+        const T *buf = (b & 1) ? stage1 : stage;
         if (!upper) {
-            // columns c0..c0+P-1 of A, rows c..n-1 (lower part only)
-            if (live)
-                for (int cc = sc; cc < P; cc += CT) {
-                    const int c = c0 + cc;
-                    if (c >= n) break;
-                    for (int r = c + sr; r < n; r += RT) stage[cc * LDST + r] = A[static_cast<int64_t>(c) * lda + r];
-                }
-            tile_sync<WS>();
             const int c = c0 + q;
 #pragma unroll
             for (int s = b; s < S; ++s) {
                 const int i = p + P * s;
-                if (c < n && i < n && (s > b || p >= q)) a[s][b] = stage[q * LDST + i];
+                if (c < n && i < n && (s > b || p >= q)) a[s][b] = buf[q * LDST + i];
             }
         } else {
-            // rows c0..c0+P-1 of S = columns of A, A rows 0..i (upper part only)
-            if (live)
-                for (int ii = sc; ii < P; ii += CT) {
-                    const int i = c0 + ii;
-                    if (i >= n) break;
-                    for (int k = sr; k <= i; k += RT) stage[ii * LDST + k] = A[static_cast<int64_t>(i) * lda + k];
-                }
-            tile_sync<WS>();
             const int i = c0 + p;
 #pragma unroll
             for (int t = 0; t <= b; ++t) {
                 const int k = q + P * t;
-                if (i < n && (t < b || q <= p)) a[b][t] = conj(stage[p * LDST + k]);
+                if (i < n && (t < b || q <= p)) a[b][t] = conj(buf[p * LDST + k]);
             }
         }
         tile_sync<WS>();
     }
+    cp_async_wait_all();
     // right-hand sides as conjugated extra rows: entry (N-1-c, k) = conj(B(k, c))
     if (nrhs > 0 && live && xrow) {
 #pragma unroll

@@ -17,15 +17,14 @@ from matrix_dense_linear_spd_gb300 import build
 EXCEPTIONS = {
     # the f32 column-block tensor-core kernel (Lower view): 255 registers, one 8-byte value spilled
     "_ZN2bl15colblock_kernelIfLb0EEEvNS_9BatchArgsE": (8, 8, 8),
-    # register-tile kernels: ptxas caps their registers for occupancy and spills one to six words;
-    # a minimum of one CTA per SM removes the spill but raises the registers and halves the
+    # register-tile kernels: ptxas caps their registers for occupancy and spills one to seven
+    # words; a minimum of one CTA per SM removes the spill but raises the registers and halves the
     # occupancy of the larger tiles (c64 n=128 on tile:p=16:s=8: 1.96 -> 3.19 ms), so they keep
-    # the cap
-    "_ZN2bl11tile_kernelIfLi16ELi6EEEvNS_9BatchArgsE": (8, 4, 4),
-    "_ZN2bl11tile_kernelIfLi8ELi8EEEvNS_9BatchArgsE": (8, 8, 8),
-    "_ZN2bl11tile_kernelIfLi8ELi6EEEvNS_9BatchArgsE": (16, 12, 12),
+    # the cap. With the double-buffered cp.async staging the f32 16 x 8 tile spills 28 bytes at 64
+    # registers and still runs faster than before it (f32 n=128 b8192: 0.888 -> 0.834 ms)
+    "_ZN2bl11tile_kernelIfLi16ELi8EEEvNS_9BatchArgsE": (24, 28, 28),
     "_ZN2bl11tile_kernelINS_4cf32ELi8ELi8EEEvNS_9BatchArgsE": (16, 24, 24),
-    "_ZN2bl11tile_kernelINS_4cf32ELi8ELi6EEEvNS_9BatchArgsE": (8, 4, 4),
+    "_ZN2bl11tile_kernelINS_4cf32ELi4ELi8EEEvNS_9BatchArgsE": (8, 8, 8),
     # float2-row kernel, 8 lanes x 4 rows (four matrices per warp, compacted slabs): 80 words of
     # rows per lane; it spills at every bound tried (128, 168 and 255 registers; also with the
     # prefetch or the Upper path compiled out), the least at these. The factor-only kernel loses
