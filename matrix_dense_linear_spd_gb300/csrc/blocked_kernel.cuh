@@ -150,12 +150,21 @@ __global__ void __launch_bounds__(256, sizeof(T) >= 16 ? 2 : 4) blocked_kernel(c
             const int ntile = (mt + TB - 1) / TB;
             T *sI = sW;
             T *sK = sW + NB * LDT;
-            const int ti = upper ? tid / 16 : tid % 16;   // row group (4 rows)
-            const int tk = upper ? tid % 16 : tid / 16;   // column group (4 columns)
+            // a thread owns a 4 x 4 block (row group ti, column group tk) of the 64 x 64 tile; warp
+            // w owns rows 16*(w%4) .. +15 and columns 32*(w/4) .. +31, so a warp whose whole patch
+            // lies above a diagonal tile's diagonal or past the matrix's last row or column skips
+            // the tile (2 of 8 warps on every diagonal tile; the half-empty last row of tiles when
+            // the trailing order is an odd multiple of 32). Inside the warp the index that is
+            // contiguous in memory varies fastest across lanes (Lower: rows; Upper: columns of S)
+            const int wrp = tid >> 5, ln = tid & 31;
+            const int rg = wrp & 3, cg = wrp >> 2;
+            const int ti = 4 * rg + (upper ? ln / 8 : ln % 4);    // row group (4 rows)
+            const int tk = 8 * cg + (upper ? ln % 8 : ln / 4);    // column group (4 columns)
             for (int bi = 0; bi < ntile; ++bi) {
                 const int I0 = m0 + bi * TB;
                 for (int bk = 0; bk <= bi; ++bk) {
                     const int K0 = m0 + bk * TB;
+                    const bool idle = I0 + 16 * rg >= n || K0 + 32 * cg >= n || (bi == bk && 16 * rg + 15 < 32 * cg);
                     for (int idx = tid; idx < kb * TB; idx += THREADS) {
                         const int a0 = upper ? idx % kb : idx % TB;
                         const int a1 = upper ? idx / kb : idx / TB;
@@ -164,35 +173,36 @@ __global__ void __launch_bounds__(256, sizeof(T) >= 16 ? 2 : 4) blocked_kernel(c
                         sK[c * LDT + rr] = (K0 + rr < n) ? S.get(K0 + rr, j0 + c) : zero<T>();
                     }
                     __syncthreads();
-                    T acc[4][4];
-#pragma unroll
-                    for (int a = 0; a < 4; ++a)
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) acc[a][b] = zero<T>();
-                    for (int c = 0; c < kb; ++c) {
-                        T u[4], v[4];
-#pragma unroll
-                        for (int a = 0; a < 4; ++a) u[a] = sI[c * LDT + 4 * ti + a];
-#pragma unroll
-                        for (int b = 0; b < 4; ++b) v[b] = sK[c * LDT + 4 * tk + b];
+                    if (!idle) {                  // warp-uniform: skip a wholly masked patch
+                        T acc[4][4];
 #pragma unroll
                         for (int a = 0; a < 4; ++a)
 #pragma unroll
-                            for (int b = 0; b < 4; ++b) sub_mul_conj(acc[a][b], u[a], v[b]);
-                    }
-                    // acc = -L21_I L21_K^H; add into the trailing matrix, lower part only
+                            for (int b = 0; b < 4; ++b) acc[a][b] = zero<T>();
+                        for (int c = 0; c < kb; ++c) {
+                            T u[4], v[4];
 #pragma unroll
-                    for (int b = 0; b < 4; ++b)
+                            for (int a = 0; a < 4; ++a) u[a] = sI[c * LDT + 4 * ti + a];
 #pragma unroll
-                        for (int a = 0; a < 4; ++a) {
-                            const int i = I0 + 4 * ti + a, k = K0 + 4 * tk + b;
-                            if (i < n && k < n && i >= k) {
-                                T v = S.get(i, k);
-                                add_into(v, acc[a][b]);   // acc holds -sum
-
-                                S.set(i, k, v);
-                            }
+                            for (int b = 0; b < 4; ++b) v[b] = sK[c * LDT + 4 * tk + b];
+#pragma unroll
+                            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                                for (int b = 0; b < 4; ++b) sub_mul_conj(acc[a][b], u[a], v[b]);
                         }
+                        // acc = -L21_I L21_K^H; add into the trailing matrix, lower part only
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+#pragma unroll
+                            for (int a = 0; a < 4; ++a) {
+                                const int i = I0 + 4 * ti + a, k = K0 + 4 * tk + b;
+                                if (i < n && k < n && i >= k) {
+                                    T v = S.get(i, k);
+                                    add_into(v, acc[a][b]);   // acc holds -sum
+                                    S.set(i, k, v);
+                                }
+                            }
+                    }
                     __syncthreads();
                 }
             }
