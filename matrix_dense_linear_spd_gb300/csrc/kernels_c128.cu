@@ -9,6 +9,8 @@ static const KernelEntry k_entries_c128[] = {
     thread_entry<cf64, 8>(),
     thread_entry<cf64, 12>(),
     thread_entry<cf64, 18>(),
+    thread_entry<cf64, 12, 2>(),
+    thread_entry<cf64, 18, 2>(),
     warp_entry<cf64, 4, 2>(),
     warp_entry<cf64, 8, 1>(),
     warp_entry<cf64, 16, 1>(),

@@ -276,6 +276,34 @@ def test_edge_cases_and_argument_errors():
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("dtype", ["f64", "c128"])
+def test_lane_pair_thread_routes_are_bit_identical(dtype):
+    """thread:n=N:p=2 (two lanes per matrix, each summing one parity of k, added in the same
+    order) gives the bits and info of thread:n=N, also with failing pivots at odd and even
+    columns and a NaN, for Lower and Upper and orders below the capacity."""
+    bl = lib()
+    rng = np.random.default_rng(41)
+    routes = {sp: cap for sp, cap, _ in bl.routes(dtype)}
+    for sp, cap in routes.items():
+        if not sp.startswith("thread:") or ":p=2" not in sp:
+            continue
+        base = sp.replace(":p=2", "")
+        assert base in routes, base
+        for n in sorted({cap, cap - 1, max(1, cap - 6)}):
+            A = synth.spd_bbt(rng, n, 131, dtype)
+            A[3, n - 1, n - 1] = -1.0
+            A[4, n // 2, n // 2] = -1.0
+            A[5, (n - 1) // 3, (n - 1) // 3] = np.nan
+            for uplo in "LU":
+                o0, i0, _ = _check_potrf(A, uplo, dtype, route=base)
+                o1, i1, _ = _check_potrf(A, uplo, dtype, route=sp)
+                assert np.array_equal(i0, i1), (sp, n, uplo)
+                f0, f1 = synth.from_colmajor(o0, n, n, 131), synth.from_colmajor(o1, n, n, 131)
+                ok = i0 == 0
+                assert np.array_equal(np.ascontiguousarray(f0[ok]).view(np.uint8),
+                                      np.ascontiguousarray(f1[ok]).view(np.uint8)), (sp, n, uplo)
+
+
 def test_pair_row_routes_leave_the_other_triangle():
     """Every float2-pair-row route, pinned: NaN in the other triangle changes no bit of the
     factor (its slab copy and pick read only the referenced triangle's values into the factor)
