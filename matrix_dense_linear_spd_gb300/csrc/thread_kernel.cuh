@@ -93,7 +93,19 @@ __global__ void __launch_bounds__(ThreadCfg<T, NMAX, TPMX>::THREADS, 1) thread_k
     // flat index idx = mm * nn + rem over the CTA's items, walked in steps of THREADS without division
     const int dm = THREADS / nn, dr = THREADS - (THREADS / nn) * nn;
     const T *A = static_cast<const T *>(args.A) + m0 * sa;
-    {
+    // items stored back to back (lda = n, stride = n^2): the global offset is the flat index
+    // itself, so the walk needs no 64-bit index arithmetic per element
+    const bool flat = lda == n && sa == nn;
+    if (flat) {
+        int mb = (tid / nn) * PACK, rem = tid - (tid / nn) * nn;
+        for (int idx = tid; idx < nm * nn; idx += THREADS) {
+            const uint32_t slot = tab[rem] & 0xFFFFu;
+            if (slot != 0xFFFFu) cp_async_elem<sizeof(T)>(sm + mb + slot, A + idx);
+            mb += dm * PACK;
+            rem += dr;
+            if (rem >= nn) rem -= nn, mb += PACK;
+        }
+    } else {
         int mm = tid / nn, rem = tid - (tid / nn) * nn;
         for (int idx = tid; idx < nm * nn; idx += THREADS) {
             const uint32_t e = tab[rem];
@@ -259,7 +271,19 @@ __global__ void __launch_bounds__(ThreadCfg<T, NMAX, TPMX>::THREADS, 1) thread_k
 
     // ---- store of the referenced triangles, same walk (coalesced global writes)
     T *Aw = static_cast<T *>(args.A) + m0 * sa;
-    {
+    if (flat) {
+        int mb = (tid / nn) * PACK, rem = tid - (tid / nn) * nn;
+        for (int idx = tid; idx < nm * nn; idx += THREADS) {
+            const uint32_t slot = tab[rem] & 0xFFFFu;
+            if (slot != 0xFFFFu) {
+                const T v = sm[mb + slot];
+                Aw[idx] = upper ? conj(v) : v;
+            }
+            mb += dm * PACK;
+            rem += dr;
+            if (rem >= nn) rem -= nn, mb += PACK;
+        }
+    } else {
         int mm = tid / nn, rem = tid - (tid / nn) * nn;
         for (int idx = tid; idx < nm * nn; idx += THREADS) {
             const uint32_t e = tab[rem];
