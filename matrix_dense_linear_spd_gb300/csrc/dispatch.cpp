@@ -95,7 +95,8 @@ std::string spelling(const KernelEntry &e) {
     else if (e.family == 2)   // nb bit 0: whole squares, bit 1: packed f32x2 update
         snprintf(buf, sizeof buf, "warp:p=%d:r=%d%s%s%s%s", e.p, e.s, (e.nb & 1) ? ":full=1" : "", (e.nb & 2) ? ":x2=1" : "",
                  (e.nb & 4) ? ":la=1" : "", (e.nb & 8) ? ":v2=1" : "");   // bit 2: look-ahead pivots, bit 3: float2-pair rows
-    else if (e.family == 3) snprintf(buf, sizeof buf, "thread:n=%d%s", e.nb, e.p == 2 ? ":p=2" : "");   // p: lanes per matrix
+    else if (e.family == 3)   // p: lanes per matrix; e: fully unrolled at n = NMAX
+        snprintf(buf, sizeof buf, "thread:n=%d%s%s", e.nb, e.p == 2 ? ":p=2" : "", e.s == 1 ? ":e=1" : "");
     else if (e.s) snprintf(buf, sizeof buf, "blocked:nb=%d:tc=%d", e.nb, e.s);   // 2: the column-block tensor-core kernel
     else snprintf(buf, sizeof buf, "blocked:nb=%d", e.nb);
     return buf;
@@ -115,7 +116,7 @@ std::string canon(std::string s) {
     while (std::getline(ss, tok, ':')) parts.push_back(tok);
     if (parts.empty()) return s;
     static const std::map<std::string, std::vector<std::string>> fields = {
-        {"tile", {"p", "s"}}, {"warp", {"p", "r", "full", "x2", "la", "v2"}}, {"blocked", {"nb", "tc"}}, {"thread", {"n", "p"}}};
+        {"tile", {"p", "s"}}, {"warp", {"p", "r", "full", "x2", "la", "v2"}}, {"blocked", {"nb", "tc"}}, {"thread", {"n", "p", "e"}}};
     auto it = fields.find(parts[0]);
     if (it == fields.end()) return s;
     std::string out = parts[0];

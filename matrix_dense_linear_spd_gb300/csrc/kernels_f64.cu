@@ -11,6 +11,7 @@ static const KernelEntry k_entries_f64[] = {
     thread_entry<double, 18>(),
     thread_entry<double, 12, 2>(),
     thread_entry<double, 18, 2>(),
+    thread_entry<double, 17, 1, true>(),
     warp_entry<double, 4, 2>(),
     warp_entry<double, 8, 1>(),
     warp_entry<double, 4, 4>(),

@@ -172,23 +172,25 @@ constexpr KernelEntry warp_entry() {
                        C::PER_CTA, WHOLE ? C::smem_solve_full : C::smem_solve, &launch_warp<T, P, R, WHOLE, PK, LA, V2>};
 }
 
-template <typename T, int NMAX, int TPMX>
+template <typename T, int NMAX, int TPMX, bool EXACT>
 cudaError_t launch_thread(const BatchArgs &a, cudaStream_t st) {
     using C = ThreadCfg<T, NMAX, TPMX>;
     static std::atomic<unsigned long long> done{0};
-    cudaError_t e = ensure_smem(thread_kernel<T, NMAX, TPMX>, C::smem_bytes, done);
+    cudaError_t e = ensure_smem(thread_kernel<T, NMAX, TPMX, EXACT>, C::smem_bytes, done);
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>((a.batch + C::MATS - 1) / C::MATS);
-    thread_kernel<T, NMAX, TPMX><<<grid, C::THREADS, C::smem_bytes, st>>>(a);
+    thread_kernel<T, NMAX, TPMX, EXACT><<<grid, C::THREADS, C::smem_bytes, st>>>(a);
     return cudaGetLastError();
 }
 
-// TPMX = 2: a pair of lanes per matrix ("thread:n=NMAX:p=2")
-template <typename T, int NMAX, int TPMX = 1>
+// TPMX = 2: a pair of lanes per matrix ("thread:n=NMAX:p=2"); EXACT: fully unrolled at n == NMAX
+// ("thread:n=NMAX:e=1")
+template <typename T, int NMAX, int TPMX = 1, bool EXACT = false>
 constexpr KernelEntry thread_entry() {
+    static_assert(!EXACT || TPMX == 1, "the unrolled order-N factor is one lane per matrix");
     using C = ThreadCfg<T, NMAX, TPMX>;
-    return KernelEntry{3, TPMX == 1 ? 0 : TPMX, 0, NMAX, NMAX, -1, C::THREADS, C::MATS, C::smem_bytes,
-                       &launch_thread<T, NMAX, TPMX>};
+    return KernelEntry{3, TPMX == 1 ? 0 : TPMX, EXACT ? 1 : 0, NMAX, NMAX, -1, C::THREADS, C::MATS, C::smem_bytes,
+                       &launch_thread<T, NMAX, TPMX, EXACT>};
 }
 
 template <typename T, int P, int S>

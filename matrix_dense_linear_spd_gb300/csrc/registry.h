@@ -14,7 +14,8 @@ struct KernelEntry {
     int family;          // 0 = tile, 1 = blocked, 2 = warp, 3 = thread (potrf only)
     int p, s, nb;        // tile geometry (p, s), warp geometry (p lanes, s = rows per lane; nb bit 0:
                          // whole-square slabs, bit 1: packed f32x2 update), blocked panel width nb (s = 2: the column-block
-                         // tensor-core kernel), or thread capacity nb (p = 2: a pair of lanes per matrix)
+                         // tensor-core kernel), or thread capacity nb (p = 2: a pair of lanes per matrix;
+                         // s = 1: fully unrolled at n = nb)
     int cap;
     int rhs_max;
     int threads, per_cta;

@@ -57,13 +57,78 @@ struct ThreadCfg {
 
 __device__ __forceinline__ int tri_idx(int i, int j) { return i * (i + 1) / 2 + j; }
 
+// One matrix per thread at the compile-time order N: the one-thread kernel's row loop (below)
+// with every loop unrolled, so every shared-memory offset is an immediate, no loop control is
+// left and the compiler may keep row i in registers; the operations and their order are the
+// row loop's, so the results are bit-identical to it. Returns info.
+template <typename T, int N>
+__device__ __forceinline__ int factor_exact(T *a, bool upper) {
+    using R = real_t<T>;
+    R *rinv = reinterpret_cast<R *>(a + N * (N + 1) / 2);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        T *ri = a + tri_idx(i, 0);
+#pragma unroll
+        for (int j = 0; j + 1 < i; j += 2) {
+            const T *rj = a + tri_idx(j, 0);
+            const T *rj1 = rj + j + 1;
+            T sa0 = upper ? conj(ri[j]) : ri[j], sb0 = upper ? conj(ri[j + 1]) : ri[j + 1];
+            T sa1 = zero<T>(), sb1 = zero<T>();
+#pragma unroll
+            for (int k = 0; k + 1 < j; k += 2) {
+                const T x0 = ri[k], x1 = ri[k + 1];
+                sub_mul_conj(sa0, x0, rj[k]);
+                sub_mul_conj(sb0, x0, rj1[k]);
+                sub_mul_conj(sa1, x1, rj[k + 1]);
+                sub_mul_conj(sb1, x1, rj1[k + 1]);
+            }
+            add_into(sa0, sa1);                                  // j even: no odd leftover k
+            add_into(sb0, sb1);
+            const T lij = scale(sa0, rinv[j]);
+            ri[j] = lij;
+            sub_mul_conj(sb0, lij, rj1[j]);
+            ri[j + 1] = scale(sb0, rinv[j + 1]);
+        }
+        if (i & 1) {                                             // leftover entry j = i-1 (even)
+            const int j = i - 1;
+            const T *rj = a + tri_idx(j, 0);
+            T s0 = upper ? conj(ri[j]) : ri[j], s1 = zero<T>();
+#pragma unroll
+            for (int k = 0; k + 1 < j; k += 2) {
+                sub_mul_conj(s0, ri[k], rj[k]);
+                sub_mul_conj(s1, ri[k + 1], rj[k + 1]);
+            }
+            add_into(s0, s1);
+            ri[j] = scale(s0, rinv[j]);
+        }
+        R d0 = re(ri[i]), d1 = R(0), d2 = R(0), d3 = R(0);
+#pragma unroll
+        for (int k = 0; k + 3 < i; k += 4) {
+            sub_abs2(d0, ri[k]);
+            sub_abs2(d1, ri[k + 1]);
+            sub_abs2(d2, ri[k + 2]);
+            sub_abs2(d3, ri[k + 3]);
+        }
+#pragma unroll
+        for (int k = (i / 4) * 4; k < i; ++k) sub_abs2(d0, ri[k]);
+        const R dd = (d0 + d1) + (d2 + d3);
+        if (!(dd > R(0))) return i + 1;
+        const R r = rsqrt_of(dd);
+        ri[i] = from_real<T>(dd * r);
+        rinv[i] = r;
+    }
+    return 0;
+}
+
 // The value of the other lane of an adjacent-lane pair (mask m names the pair's two lanes).
 __device__ __forceinline__ double shfl_xor_pair(double v, unsigned m) { return __shfl_xor_sync(m, v, 1); }
 __device__ __forceinline__ cf64 shfl_xor_pair(cf64 v, unsigned m) {
     return cf64{__shfl_xor_sync(m, v.x, 1), __shfl_xor_sync(m, v.y, 1)};
 }
 
-template <typename T, int NMAX, int TPMX = 1>
+// EXACT: when n == NMAX the one-thread factor runs fully unrolled (factor_exact); other orders
+// run the row loop.
+template <typename T, int NMAX, int TPMX = 1, bool EXACT = false>
 __global__ void __launch_bounds__(ThreadCfg<T, NMAX, TPMX>::THREADS, 1) thread_kernel(const BatchArgs args) {
     using C = ThreadCfg<T, NMAX, TPMX>;
     using R = real_t<T>;
@@ -127,7 +192,14 @@ __global__ void __launch_bounds__(ThreadCfg<T, NMAX, TPMX>::THREADS, 1) thread_k
         // ---- one matrix per thread. Two entries of row i at a time (j, j+1): the shared loads of
         // L(i,k) feed both dot products, and each is split in two partial sums, so four independent
         // FP64 chains are in flight per thread (the FP64 pipe's latency is long).
-        if (tid < nm) {
+        bool done = false;
+        if constexpr (EXACT) {
+            if (tid < nm && n == NMAX) {
+                info = factor_exact<T, NMAX>(sm + tid * PACK, upper);
+                done = true;
+            }
+        }
+        if (tid < nm && !done) {
             T *a = sm + tid * PACK;
             R *rinv = reinterpret_cast<R *>(a + TRI);
             for (int i = 0; i < n; ++i) {

@@ -279,15 +279,18 @@ def test_edge_cases_and_argument_errors():
 @pytest.mark.parametrize("dtype", ["f64", "c128"])
 def test_lane_pair_thread_routes_are_bit_identical(dtype):
     """thread:n=N:p=2 (two lanes per matrix, each summing one parity of k, added in the same
-    order) gives the bits and info of thread:n=N, also with failing pivots at odd and even
-    columns and a NaN, for Lower and Upper and orders below the capacity."""
+    order) gives the bits and info of thread:n=N, and thread:n=N:e=1 (fully unrolled at n = N)
+    those of the row loop, also with failing pivots at odd and even columns and a NaN, for Lower
+    and Upper and orders below the capacity."""
     bl = lib()
     rng = np.random.default_rng(41)
     routes = {sp: cap for sp, cap, _ in bl.routes(dtype)}
+    general = max((c, r) for r, c in routes.items() if r.startswith("thread:") and ":" not in r[7:])[1]
     for sp, cap in routes.items():
-        if not sp.startswith("thread:") or ":p=2" not in sp:
+        if not sp.startswith("thread:") or (":p=2" not in sp and ":e=1" not in sp):
             continue
-        base = sp.replace(":p=2", "")
+        # the unrolled order-N path against the row loop of the widest one-lane route
+        base = sp.replace(":p=2", "") if ":p=2" in sp else general
         assert base in routes, base
         for n in sorted({cap, cap - 1, max(1, cap - 6)}):
             A = synth.spd_bbt(rng, n, 131, dtype)
