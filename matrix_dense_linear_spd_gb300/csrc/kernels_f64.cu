@@ -11,7 +11,11 @@ static const KernelEntry k_entries_f64[] = {
     thread_entry<double, 18>(),
     thread_entry<double, 12, 2>(),
     thread_entry<double, 18, 2>(),
+    thread_entry<double, 8, 1, true>(),
+    thread_entry<double, 12, 1, true>(),
+    thread_entry<double, 16, 1, true>(),
     thread_entry<double, 17, 1, true>(),
+    thread_entry<double, 18, 1, true>(),
     warp_entry<double, 4, 2>(),
     warp_entry<double, 8, 1>(),
     warp_entry<double, 4, 4>(),
