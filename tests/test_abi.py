@@ -246,3 +246,27 @@ def test_column_block_and_packed_routes_parse_and_select(bl):
     assert bl.select_debug("potrf", "f32", "L", 512, 0, 1024).startswith("blocked:nb=32:tc=2")
     assert bl.select_debug("potrf", "f32", "U", 512, 0, 1024).startswith("blocked:nb=32:tc=2")
     assert bl.select_debug("posv", "f32", "L", 512, 8, 1024).startswith("blocked:nb=32 ")
+
+
+def test_thread_variants_parse_and_select(bl):
+    """The thread-per-matrix variants -- a lane pair per matrix (thread:n=N:p=2, f64 and c128)
+    and fully unrolled at one order (thread:n=N:e=1, f64) -- are compiled, pinnable by their
+    spellings (also positionally), refused above their order and for posv (factor only), and
+    the shipped f64 table picks the unrolled order-17 variant for the n=17 configuration."""
+    f64 = {sp: (cap, rhs) for sp, cap, rhs in bl.routes("f64")}
+    c128 = {sp: (cap, rhs) for sp, cap, rhs in bl.routes("c128")}
+    assert f64["thread:n=18:p=2"] == (18, -1) and c128["thread:n=18:p=2"] == (18, -1)
+    assert f64["thread:n=17:e=1"] == (17, -1)
+    assert not any(":e=1" in sp for sp in c128)
+    for op, sp, n, ok in (("potrf", "thread:n=17:e=1", 17, True), ("potrf", "thread:n=17:e=1", 18, False),
+                          ("potrf", "thread:n=17:e=1", 9, True), ("posv", "thread:n=17:e=1", 17, False),
+                          ("potrf", "THREAD:18:2", 18, True), ("potrf", "thread:n=18:p=2", 19, False)):
+        bl.set_route(op, sp)
+        try:
+            out = bl.select_debug(op, "f64", "L", n, 4 if op == "posv" else 0, 4096)
+            assert out.startswith("error:") != ok, (op, sp, n, out)
+            if ok:
+                assert out.startswith("thread:n=17:e=1" if ":e=1" in sp else "thread:n=18:p=2"), out
+        finally:
+            bl.set_route(op, None)
+    assert bl.select_debug("potrf", "f64", "L", 17, 0, 32768).startswith("thread:n=17:e=1")
