@@ -17,8 +17,13 @@
 // Data movement: the CTA's triangles arrive by asynchronous element copies (cp.async, no
 // register round trip, all in flight at once) in global-address order, so a warp's copies are
 // coalesced; a per-CTA table maps each position of an n x n item to its packed slot, so the
-// copy loop needs no division. The packed stride is odd in 8-byte words, so the per-thread
-// accesses of the factorisation are bank-conflict free.
+// copy loop needs no division, and for items stored back to back the global offset is the flat
+// index itself. The per-matrix stride keeps the factorisation's shared-memory accesses
+// bank-conflict free (see ThreadCfg).
+//
+// Variants: a pair of lanes per matrix (TPMX = 2), each lane summing one parity of every dot
+// product; and the one-lane factor fully unrolled at n == NMAX (EXACT). Both perform the row
+// loop's operations in the row loop's order, so all variants give the same bits.
 #pragma once
 
 #include "bl_types.cuh"
