@@ -108,6 +108,18 @@ def read_ledger(path):
         return [json.loads(x) for x in f if x.strip()]
 
 
+LEDGER_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tuned", "ledger")
+
+
+def shipped_ledgers(op):
+    """The committed ledgers of `op` (tuned/ledger/<op>_run<k>.jsonl.gz), in run order; the
+    shipped table of `op` is their verdict."""
+    import glob
+    import re
+    files = glob.glob(os.path.join(LEDGER_DIR, f"{op}_run*.jsonl.gz"))
+    return sorted(files, key=lambda p: int(re.search(r"_run(\d+)\.", os.path.basename(p)).group(1)))
+
+
 def write_tables(ledger_path, out_dir, devkey=None):
     recs = []
     for p in ledger_path.split(","):
@@ -242,6 +254,8 @@ def main(argv=None):
     ap.add_argument("--out", required=True)
     ap.add_argument("--max-seconds", type=float, default=1e9)
     ap.add_argument("--tables-from", default=None, help="only regenerate tables from these ledgers (comma list)")
+    ap.add_argument("--regenerate", action="store_true",
+                    help="only regenerate both tables from every committed ledger (tuned/ledger), into --out")
     ap.add_argument("--cells", default=None,
                     help="explicit cells instead of the grid: dtype:uplo:n:batch[:nrhs] separated by commas")
     ap.add_argument("--min-n", type=int, default=0, help="skip grid points below this n")
@@ -250,6 +264,11 @@ def main(argv=None):
     if a.tables_from:
         for p in write_tables(a.tables_from, a.out):
             print(p)
+        return 0
+    if a.regenerate:
+        for op in ("potrf", "posv"):
+            for p in write_tables(",".join(shipped_ledgers(op)), a.out):
+                print(p)
         return 0
     import torch
     import matrix_dense_linear_spd_gb300 as bl

@@ -78,3 +78,18 @@ print(bl.select_debug("potrf", "f32", "L", 8, 0, 16384, devkey="sm_999"))
     a, b = out.stdout.strip().splitlines()
     assert a.startswith("tile:p=4:s=8 [table override sm_999 row n=32 batch=16384]")
     assert b.startswith("warp:p=16:r=2 [table override sm_999 row n=8 batch=16384]")
+
+
+def test_shipped_tables_are_the_verdict_of_the_committed_ledgers(tmp_path):
+    """Every shipped table row is what the ledger -> table step makes of the committed ledgers
+    (tuned/ledger, all runs, the latest measurement of a cell and candidate winning): the tables
+    are reproducible from the measurements alone (only the header's date may differ)."""
+    import re
+    tuned = os.path.join(os.path.dirname(sweep.__file__), "tuned")
+    for op in ("potrf", "posv"):
+        ledgers = sweep.shipped_ledgers(op)
+        assert ledgers, op
+        (path,) = sweep.write_tables(",".join(ledgers), str(tmp_path))
+        got = open(path).read()
+        shipped = open(os.path.join(tuned, f"{op}.sm_103.txt")).read()
+        assert re.sub(r"date=\S+", "", got) == re.sub(r"date=\S+", "", shipped), op
