@@ -93,3 +93,31 @@ def test_shipped_tables_are_the_verdict_of_the_committed_ledgers(tmp_path):
         got = open(path).read()
         shipped = open(os.path.join(tuned, f"{op}.sm_103.txt")).read()
         assert re.sub(r"date=\S+", "", got) == re.sub(r"date=\S+", "", shipped), op
+
+
+# (op, dtype, uplo, n, nrhs, batch) of every configuration the benchmark and the report time
+CONFIG_CELLS = [
+    ("potrf", "f32", "L", 8, 0, 1024), ("potrf", "f32", "L", 32, 0, 16384), ("potrf", "f32", "U", 32, 0, 16384),
+    ("posv", "f32", "L", 32, 4, 16384), ("potrf", "f64", "L", 17, 0, 32768), ("potrf", "f64", "L", 33, 0, 16384),
+    ("potrf", "f64", "L", 65, 0, 8192), ("potrf", "c64", "L", 128, 0, 8192), ("posv", "c64", "L", 128, 8, 8192),
+    ("potrf", "f32", "L", 512, 0, 1024), ("potrf", "f64", "L", 512, 0, 1024), ("posv", "f64", "L", 512, 8, 1024),
+]
+
+
+def test_every_configuration_is_a_measured_row_and_selects_its_winner():
+    """Each configuration's own (dtype, uplo, n[, nrhs], batch) is a measured row of the shipped
+    table (not a nearest-row borrow), and the selection layer picks that row's winner there."""
+    import matrix_dense_linear_spd_gb300 as bl
+    tuned = os.path.join(os.path.dirname(sweep.__file__), "tuned")
+    rows = {}
+    for op in ("potrf", "posv"):
+        for line in open(os.path.join(tuned, f"{op}.sm_103.txt")):
+            if line.startswith("#"):
+                continue
+            key, rest = line.split("|", 1)
+            rows[(op, key.strip())] = rest.split("|")[0].strip().rsplit(" ", 1)[0]
+    for op, dt, uplo, n, nrhs, batch in CONFIG_CELLS:
+        key = f"dtype={dt} uplo={uplo} n={n}" + (f" nrhs={nrhs}" if op == "posv" else "") + f" batch={batch}"
+        assert (op, key) in rows, (op, key)
+        chosen = bl.select_debug(op, dt, uplo, n, nrhs, batch)
+        assert chosen.split(" ")[0] == rows[(op, key)], (op, key, chosen)
