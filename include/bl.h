@@ -128,8 +128,10 @@ int bl_num_routes(bl_dtype dtype);
 const char *bl_route_name(bl_dtype dtype, int i);
 
 /* Capacity of variant i: returns the largest order it holds (for "tile" variants: n plus the
- * right-hand sides of one pass; for "warp" variants: n), 0 for "any order", or -1 when i is out
- * of range; *rhs_per_pass receives the right-hand sides one pass solves (0 = any). */
+ * right-hand sides of one pass; for "warp" and "thread" variants: n; "thread:n=N:e=1" runs its
+ * unrolled path at n = N and the general one below), 0 for "any order", or -1 when i is out of
+ * range; *rhs_per_pass receives the right-hand sides one pass solves (0 = any, -1 = the variant
+ * factors only: potrf, not posv or potrs). */
 int bl_route_capacity(bl_dtype dtype, int i, int *rhs_per_pass);
 
 /*
